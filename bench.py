@@ -1,0 +1,396 @@
+"""Benchmark: ReplaySSM decode of a Nemotron-shaped Mamba-2 layer on GB300.
+
+Workload (per GPU): batch 256, 128 heads, headdim 64, dstate 128, 8 groups, bf16 inputs,
+FP32 checkpoint, window L = 16; synthetic seeded inputs of the layer's distributions.
+One bench step = one window of L decode tokens for the whole batch (15 non-flush steps and
+one flush), i.e. batch * L tokens. The 1 GiB checkpoint is larger than the 129 MB L2, so no
+L2 flush is needed between steps.
+
+``python bench.py [--gpus N --steps K --warmup W]`` prints one JSON line. Under torchrun
+every rank decodes its own batch (weak scaling, no collective on the data path); value is
+all ranks' tokens over the slowest rank's time. ``--impl reference`` times the FP64 oracle
+on the host cores on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = pathlib.Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import synthgen as sg  # noqa: E402
+
+METRIC = "replay decode tokens/s & achieved HBM GB/s (vs ~8 TB/s), batch 256, L=16"
+UNIT = "tokens/s"
+WORKLOAD = dict(batch=256, nheads=128, headdim=64, dstate=128, ngroups=8, dtype="bf16", L=16)
+PROFILE_TRAFFIC = ROOT / "profiles" / "replay_step_nemotron_b256.md"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ algorithmic bytes
+def record_bytes(w, esz):
+    """Bytes of one input record (x, B, dt) of one sequence."""
+    return (w["nheads"] * w["headdim"] + w["ngroups"] * w["dstate"] + w["nheads"]) * esz
+
+
+def step_bytes(w, n_prior: int, flush: bool, esz=2, state_bytes=4, rc_bytes=0):
+    """Algorithmic HBM bytes of one replay_step launch over the batch.
+
+    Reads: the checkpoint (FP32, or the read copy on a non-flush step), the n_prior
+    buffered records, this token's inputs (x, B, C, dt). Writes: y (FP32) and either the
+    appended record (non-flush) or the new checkpoint (+ read copy) (flush).
+    """
+    b, H, P, N, G = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+    S = b * H * P * N
+    rec = b * record_bytes(w, esz)
+    inputs = b * (H * P + 2 * G * N + H) * esz
+    y = b * H * P * 4
+    if flush:
+        return S * state_bytes + n_prior * rec + inputs + y + S * (state_bytes + rc_bytes) + \
+            (b * H * 4 if rc_bytes == 1 else 0)
+    read = S * (rc_bytes if rc_bytes else state_bytes) + (b * H * 4 if rc_bytes == 1 else 0)
+    return read + n_prior * rec + inputs + y + rec
+
+
+def conv_bytes(w, esz=2, state_bytes=4):
+    b, H, P, N, G = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+    S = b * H * P * N
+    return 2 * S * state_bytes + b * (H * P + 2 * G * N + H) * esz + b * H * P * 4
+
+
+# ------------------------------------------------------------------ peaks and clocks
+def hbm_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    csrc = ROOT / "hybrid_model_ssm_mamba_gb300" / "csrc"
+    for p in sorted(csrc.glob("*")):
+        if p.suffix in (".cu", ".cuh", ".h"):
+            h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if taken on these sources."""
+    if not PROFILE_TRAFFIC.exists():
+        return None
+    vals = {}
+    for line in PROFILE_TRAFFIC.read_text().splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_sources_sha256") != kernel_sources_sha():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks during the timed region."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 8 or (self.uuid and self.uuid not in f[0]):
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ the replay arm
+def window_inputs(shape, seed, L, torch):
+    """L tokens of inputs on the device (one per position in the window) + pinned copies."""
+    d = sg.token_inputs(shape, seed, np.arange(L))
+    dev, host = [], []
+    for t in range(L):
+        ins = []
+        for k in ("x", "B", "C", "dt"):
+            a = np.ascontiguousarray(d[k].store[:, t])
+            ht = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+            host.append(ht)
+            ins.append(ht.to("cuda", non_blocking=False))
+        dev.append(ins)
+    return dev, [host[4 * t: 4 * t + 4] for t in range(L)]
+
+
+def run_replay(args, rank, world, local_rank):
+    import torch
+    from hybrid_model_ssm_mamba_gb300 import replay as R
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    w = WORKLOAD
+    L = w["L"]
+    shape = sg.LayerShape(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["dtype"])
+    A, D = sg.head_params(w["nheads"], 0)
+    cfg = R.ReplayConfig(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], L, 0,
+                         R.REPLAY_BF16, R.REPLAY_RC_NONE)
+    st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
+    dev, host = window_inputs(shape, rank, L, torch)
+    y = torch.empty(w["batch"], w["nheads"], w["headdim"], device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def window(events=None):
+        for t in range(L):
+            if events is not None:
+                events[t][0].record(stream)
+            st.step(*dev[t], y)
+            if events is not None:
+                events[t][1].record(stream)
+
+    for _ in range(args.warmup):
+        window()
+    torch.cuda.synchronize()
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = str(getattr(torch.cuda.get_device_properties(local_rank), "uuid", ""))
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        t0.record(stream)
+        for k in range(args.steps):
+            window(ev[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed = t0.elapsed_time(t1) / 1e3
+    launch_s = np.array([[ev[k][t][0].elapsed_time(ev[k][t][1]) / 1e3 for t in range(L)]
+                         for k in range(args.steps)])
+    assert st.status() == 0
+    elapsed_max = max_over_ranks(elapsed, world, "cuda")
+    tokens = world * w["batch"] * L * args.steps
+
+    # roofline of replay_step: algorithmic bytes of every launch / its event-timed duration
+    per_pos = [step_bytes(w, t, flush=(t == L - 1)) for t in range(L)]
+    alg_bytes = sum(per_pos) * args.steps
+    kern_s = launch_s.sum()
+    peak, peak_kind = hbm_peak()
+    achieved = alg_bytes / kern_s / 1e9
+    nf_bytes = sum(per_pos[:-1]) * args.steps
+    nf_s = launch_s[:, :-1].sum()
+    traffic = recorded_traffic()
+
+    # e2e: inputs from pinned host memory, outputs back to pinned host memory, every token
+    y_host = [torch.empty(w["batch"], w["nheads"], w["headdim"], pin_memory=True) for _ in range(L)]
+    stage = [[torch.empty_like(t) for t in ins] for ins in dev]
+
+    def e2e_window():
+        for t in range(L):
+            for dst, src in zip(stage[t], host[t]):
+                dst.copy_(src, non_blocking=True)
+            st.step(*stage[t], y)
+            y_host[t].copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_window()
+    e_steps = max(1, min(args.steps, 50))
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_window()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_el = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, "cuda")
+    h2d = sum(t.numel() * t.element_size() for ins in host for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in y_host)
+
+    # the conventional load-update-store baseline on the same workload
+    state = torch.zeros(w["batch"], w["nheads"], w["headdim"], w["dstate"], device="cuda")
+    for t in range(L):
+        R.conv_step(cfg, state, R.REPLAY_F32, st.A, st.D, *dev[t], y)
+    c_steps = max(1, min(args.steps, 20))
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(stream)
+    for _ in range(c_steps):
+        for t in range(L):
+            R.conv_step(cfg, state, R.REPLAY_F32, st.A, st.D, *dev[t], y)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    conv_s = c0.elapsed_time(c1) / 1e3 / (c_steps * L)
+    conv_tps = w["batch"] / conv_s
+
+    result = {
+        "metric": METRIC, "value": tokens / elapsed_max, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "Nemotron-shaped Mamba-2 layer decode, ReplaySSM window",
+                   "batch_per_gpu": w["batch"], "nheads": w["nheads"], "headdim": w["headdim"],
+                   "dstate": w["dstate"], "ngroups": w["ngroups"], "window_L": L,
+                   "inputs": "bf16 x/B/C/dt, FP32 checkpoint, FP32 y",
+                   "step": f"one window = {L} decode tokens x batch (15 non-flush + 1 flush)",
+                   "l2": "1 GiB checkpoint > 129 MB L2: no flush needed",
+                   "parallelism": f"dp{world} (independent batches)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "replay_step_kernel (window average)",
+                     "algorithmic_bytes_per_launch": alg_bytes / (args.steps * L),
+                     "nonflush_achieved": nf_bytes / nf_s / 1e9,
+                     "nonflush_frac": nf_bytes / nf_s / 1e9 / peak},
+        "e2e": {"value": world * w["batch"] * L * e_steps / e_el, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * L,
+        "baselines": {"conv_step_tokens_per_s": conv_tps,
+                      "conv_step_achieved_gbs": conv_bytes(w) / conv_s / 1e9,
+                      "replay_speedup_vs_conv": (w["batch"] * L * args.steps / elapsed) / conv_tps},
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_sample_seqs, args.cpu_sample_tokens)
+    st.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ------------------------------------------------------------------ the oracle (CPU)
+def oracle_tokens_per_s(n_seqs: int, n_tokens: int, seed: int = 0):
+    """Time the FP64 oracle decoding n_tokens of n_seqs sequences of the workload (all
+    heads); inputs are drawn before the clock starts."""
+    from oracle.mamba2 import Mamba2Decoder
+    w = WORKLOAD
+    shape = sg.LayerShape(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["dtype"])
+    A, D = sg.head_params(w["nheads"], 0)
+    seqs = np.arange(n_seqs)
+    d = sg.token_inputs(shape, seed, np.arange(n_tokens), seqs)
+    orc = Mamba2Decoder(A.astype(np.float64), D.astype(np.float64), w["ngroups"],
+                        np.zeros((n_seqs, w["nheads"], w["headdim"], w["dstate"])))
+    t0 = time.perf_counter()
+    for t in range(n_tokens):
+        orc.step(d["x"].f64[:, t], d["B"].f64[:, t], d["C"].f64[:, t], d["dt"].f64[:, t])
+    return n_seqs * n_tokens / (time.perf_counter() - t0)
+
+
+def cpu_baseline(n_seqs, n_tokens):
+    v = oracle_tokens_per_s(n_seqs, n_tokens)
+    return {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n_seqs} of 256 sequences x {n_tokens} tokens, all 128 heads (numpy FP64, one thread)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(1, 2)
+    t0 = time.perf_counter()
+    n_seqs, n_tokens = 2, 4
+    for _ in range(args.steps):
+        oracle_tokens_per_s(n_seqs, n_tokens, seed=1)
+    el = time.perf_counter() - t0
+    v = args.steps * n_seqs * n_tokens / el
+    sample = f"per step {n_seqs} sequences x {n_tokens} tokens, all 128 heads (numpy FP64, one thread)"
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "Nemotron-shaped Mamba-2 layer decode, FP64 oracle on host cores",
+                       "batch_per_gpu": WORKLOAD["batch"], "window_L": WORKLOAD["L"]},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="replayssm", choices=["replayssm", "reference"])
+    ap.add_argument("--cpu-sample-seqs", type=int, default=8)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=48)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_replay(args, rank, world, local_rank)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,83 @@
+"""Build the CUDA library in-tree: ``lib/libreplayssm.so`` for sm_103a.
+
+Each translation unit under ``csrc/`` compiles in parallel with nvcc; the objects are linked
+into one shared library with the CUDA runtime linked statically, so it loads without
+any other CUDA library on the path. Rebuilds only when a source or header is newer than
+the library. No cmake.
+"""
+from __future__ import annotations
+
+import os
+import pathlib
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = pathlib.Path(__file__).resolve().parent
+CSRC = PKG / "csrc"
+INCLUDE = PKG.parent / "include"
+LIBDIR = PKG / "lib"
+LIBNAME = "libreplayssm.so"
+SOURCES = ["abi.cu", "replay_step.cu", "replay_verify.cu", "replay_state.cu", "conv.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build the library")
+
+
+def lib_path() -> pathlib.Path:
+    return LIBDIR / LIBNAME
+
+
+def _inputs():
+    return [CSRC / s for s in SOURCES] + list(CSRC.glob("*.cuh")) + list(CSRC.glob("*.h")) + \
+        list(INCLUDE.glob("*.h")) + [pathlib.Path(__file__)]
+
+
+def up_to_date() -> bool:
+    lib = lib_path()
+    if not lib.exists():
+        return False
+    t = lib.stat().st_mtime
+    return all(p.stat().st_mtime <= t for p in _inputs())
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> pathlib.Path:
+    """Compile and link the library if needed; return its path."""
+    if not force and not ptxas_info and up_to_date():
+        return lib_path()
+    LIBDIR.mkdir(parents=True, exist_ok=True)
+    cc = nvcc()
+    extra = ["-Xptxas", "-v"] if ptxas_info else []
+
+    def compile_one(src: str):
+        obj = LIBDIR / (pathlib.Path(src).stem + ".o")
+        cmd = [cc, *ARCH, *FLAGS, *extra, "-I", str(INCLUDE), "-c", str(CSRC / src), "-o", str(obj)]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        return src, obj, r
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    for src, _, r in results:
+        if verbose or ptxas_info or r.returncode:
+            sys.stderr.write(r.stdout + r.stderr)
+        if r.returncode:
+            raise RuntimeError(f"nvcc failed on {src}")
+    tmp = LIBDIR / (LIBNAME + ".tmp")
+    cmd = [cc, *ARCH, "-shared", "-o", str(tmp), *[str(o) for _, o, _ in results]]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode:
+        sys.stderr.write(r.stdout + r.stderr)
+        raise RuntimeError("link of the library failed")
+    os.replace(tmp, lib_path())
+    return lib_path()
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))

@@ -1,0 +1,336 @@
+// Shared device code of the ReplaySSM kernels: the store view, the register tile of a
+// (sequence, head) slab, vector loads and stores for each storage type, warp reductions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/replayssm.h"
+
+namespace rssm {
+
+constexpr int kThreads = 256;  // one CTA per (sequence, head) slab: 8 warps
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCap = 64;    // ring records a sequence can hold (2 per lane)
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kE4M3Max = 448.0f;
+
+// Resident CTAs per SM the register budget is sized for: a P=64 slab tile is 8 rows x N/32
+// columns per thread, so wide states (N = 256) trade occupancy for registers.
+template <int N>
+constexpr int kMinBlocks = N >= 256 ? 2 : 4;
+
+using bf16 = __nv_bfloat16;
+
+// Everything a kernel needs to find a store's regions (passed by value).
+struct StoreView {
+  float* h0;      // [batch][H][P][N]
+  void* rc;       // read copy, bf16 or e4m3 [batch][H][P][N]
+  float* scale;   // [batch][H] (e4m3 copy)
+  void* xbuf;     // [batch][H][cap][P]
+  void* bbuf;     // [batch][G][cap][N]
+  void* dtbuf;    // [batch][H][cap]
+  int4* meta;     // [batch] {start, n, pending, 0}
+  int* arrive;    // [batch]
+  int* status;
+  const float* A;
+  const float* D;
+  int batch, H, G, hpg, L, cap;
+};
+
+// ------------------------------------------------------------------ element conversion
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
+
+// Load VEC consecutive elements (16-byte or smaller vector loads) and widen to float.
+template <int VEC>
+__device__ __forceinline__ void ldv(const float* p, float (&o)[VEC]) {
+  static_assert(VEC == 2 || VEC == 4, "vec");
+  if constexpr (VEC == 4) {
+    float4 v = *reinterpret_cast<const float4*>(p);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  } else {
+    float2 v = *reinterpret_cast<const float2*>(p);
+    o[0] = v.x; o[1] = v.y;
+  }
+}
+template <int VEC>
+__device__ __forceinline__ void ldv(const bf16* p, float (&o)[VEC]) {
+  static_assert(VEC == 2 || VEC == 4, "vec");
+  if constexpr (VEC == 4) {
+    uint2 v = *reinterpret_cast<const uint2*>(p);
+    float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v.x));
+    float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v.y));
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+  } else {
+    uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v));
+    o[0] = a.x; o[1] = a.y;
+  }
+}
+
+// Streaming (evict-first) FP32 loads for state slabs, which are read once per call.
+template <int VEC>
+__device__ __forceinline__ void ldv_stream(const float* p, float (&o)[VEC]) {
+  if constexpr (VEC == 4) {
+    float4 v = __ldcs(reinterpret_cast<const float4*>(p));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  } else {
+    float2 v = __ldcs(reinterpret_cast<const float2*>(p));
+    o[0] = v.x; o[1] = v.y;
+  }
+}
+template <int VEC>
+__device__ __forceinline__ void stv_stream(float* p, const float (&v)[VEC]) {
+  if constexpr (VEC == 4) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+  } else {
+    __stcs(reinterpret_cast<float2*>(p), make_float2(v[0], v[1]));
+  }
+}
+
+// Read-copy element types. A "pack" is VEC elements: 8 or 4 bytes (bf16), 4 or 2 (e4m3).
+template <int VEC>
+__device__ __forceinline__ void ld_bf16_stream(const bf16* p, float (&o)[VEC]) {
+  if constexpr (VEC == 4) {
+    uint2 v = __ldcs(reinterpret_cast<const uint2*>(p));
+    float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v.x));
+    float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v.y));
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+  } else {
+    unsigned int v = __ldcs(reinterpret_cast<const unsigned int*>(p));
+    float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v));
+    o[0] = a.x; o[1] = a.y;
+  }
+}
+template <int VEC>
+__device__ __forceinline__ void st_bf16_stream(bf16* p, const float (&v)[VEC]) {
+  if constexpr (VEC == 4) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<unsigned int*>(&a);
+    u.y = *reinterpret_cast<unsigned int*>(&b);
+    __stcs(reinterpret_cast<uint2*>(p), u);
+  } else {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+    __stcs(reinterpret_cast<unsigned int*>(p), *reinterpret_cast<unsigned int*>(&a));
+  }
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(unsigned short v) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
+  __half2 hh = *reinterpret_cast<__half2*>(&h);
+  return __half22float2(hh);
+}
+__device__ __forceinline__ unsigned short float2_to_e4m3x2(float a, float b) {
+  return static_cast<unsigned short>(
+      __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+template <int VEC>
+__device__ __forceinline__ void ld_e4m3_stream(const uint8_t* p, float scale, float (&o)[VEC]) {
+  if constexpr (VEC == 4) {
+    unsigned int v = __ldcs(reinterpret_cast<const unsigned int*>(p));
+    float2 a = e4m3x2_to_float2(static_cast<unsigned short>(v & 0xffffu));
+    float2 b = e4m3x2_to_float2(static_cast<unsigned short>(v >> 16));
+    o[0] = a.x * scale; o[1] = a.y * scale; o[2] = b.x * scale; o[3] = b.y * scale;
+  } else {
+    unsigned short v = __ldcs(reinterpret_cast<const unsigned short*>(p));
+    float2 a = e4m3x2_to_float2(v);
+    o[0] = a.x * scale; o[1] = a.y * scale;
+  }
+}
+// Codes are decided in FP32 with an IEEE division by the scale, as the format defines.
+template <int VEC>
+__device__ __forceinline__ void st_e4m3_stream(uint8_t* p, float scale, const float (&v)[VEC]) {
+  if constexpr (VEC == 4) {
+    unsigned int lo = float2_to_e4m3x2(__fdiv_rn(v[0], scale), __fdiv_rn(v[1], scale));
+    unsigned int hi = float2_to_e4m3x2(__fdiv_rn(v[2], scale), __fdiv_rn(v[3], scale));
+    __stcs(reinterpret_cast<unsigned int*>(p), lo | (hi << 16));
+  } else {
+    unsigned short c = float2_to_e4m3x2(__fdiv_rn(v[0], scale), __fdiv_rn(v[1], scale));
+    __stcs(reinterpret_cast<unsigned short*>(p), c);
+  }
+}
+
+// ------------------------------------------------------------------ slab register tile
+// A P x N slab is spread over 8 warps: warp w owns rows w*RPW .. w*RPW+RPW-1; in each row a
+// lane owns NVEC vectors of VEC columns, vector v at column v*32*VEC + lane*VEC. Every
+// vector load of a warp therefore covers a contiguous 32*VEC-element run of one row.
+template <int P, int N>
+struct Tile {
+  static_assert(P % kWarps == 0, "P must be a multiple of 8");
+  static_assert(N == 64 || N == 128 || N == 256, "N must be 64, 128 or 256");
+  static constexpr int RPW = P / kWarps;
+  static constexpr int VEC = N >= 128 ? 4 : 2;
+  static constexpr int NVEC = N / (32 * VEC);
+  static constexpr int E = VEC * NVEC;  // columns per lane
+  __device__ static __forceinline__ int row(int warp, int i) { return warp * RPW + i; }
+  __device__ static __forceinline__ int col(int lane, int v) { return v * 32 * VEC + lane * VEC; }
+};
+
+// Load the lane's E columns of a length-N vector (C or B), widened to float.
+template <int P, int N, class T>
+__device__ __forceinline__ void load_cols(const T* vec, int lane, float (&o)[Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+#pragma unroll
+  for (int v = 0; v < TL::NVEC; ++v) {
+    float t[TL::VEC];
+    ldv<TL::VEC>(vec + TL::col(lane, v), t);
+#pragma unroll
+    for (int e = 0; e < TL::VEC; ++e) o[v * TL::VEC + e] = t[e];
+  }
+}
+
+template <int P, int N>
+__device__ __forceinline__ void load_tile_f32(const float* slab, int warp, int lane,
+                                              float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+    for (int v = 0; v < TL::NVEC; ++v) {
+      float t[TL::VEC];
+      ldv_stream<TL::VEC>(slab + TL::row(warp, i) * N + TL::col(lane, v), t);
+#pragma unroll
+      for (int e = 0; e < TL::VEC; ++e) hv[i][v * TL::VEC + e] = t[e];
+    }
+}
+
+template <int P, int N>
+__device__ __forceinline__ void store_tile_f32(float* slab, int warp, int lane,
+                                               const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+    for (int v = 0; v < TL::NVEC; ++v) {
+      float t[TL::VEC];
+#pragma unroll
+      for (int e = 0; e < TL::VEC; ++e) t[e] = hv[i][v * TL::VEC + e];
+      stv_stream<TL::VEC>(slab + TL::row(warp, i) * N + TL::col(lane, v), t);
+    }
+}
+
+// Read-copy tile loads/stores. RC is REPLAY_RC_BF16 or REPLAY_RC_FP8E4M3.
+template <int P, int N, int RC>
+__device__ __forceinline__ void load_tile_rc(const void* rc, size_t slab, float scale, int warp,
+                                             int lane, float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+    for (int v = 0; v < TL::NVEC; ++v) {
+      float t[TL::VEC];
+      const size_t off = slab * P * N + TL::row(warp, i) * N + TL::col(lane, v);
+      if constexpr (RC == REPLAY_RC_BF16)
+        ld_bf16_stream<TL::VEC>(static_cast<const bf16*>(rc) + off, t);
+      else
+        ld_e4m3_stream<TL::VEC>(static_cast<const uint8_t*>(rc) + off, scale, t);
+#pragma unroll
+      for (int e = 0; e < TL::VEC; ++e) hv[i][v * TL::VEC + e] = t[e];
+    }
+}
+
+template <int P, int N, int RC>
+__device__ __forceinline__ void store_tile_rc(void* rc, size_t slab, float scale, int warp, int lane,
+                                              const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+    for (int v = 0; v < TL::NVEC; ++v) {
+      float t[TL::VEC];
+#pragma unroll
+      for (int e = 0; e < TL::VEC; ++e) t[e] = hv[i][v * TL::VEC + e];
+      const size_t off = slab * P * N + TL::row(warp, i) * N + TL::col(lane, v);
+      if constexpr (RC == REPLAY_RC_BF16)
+        st_bf16_stream<TL::VEC>(static_cast<bf16*>(rc) + off, t);
+      else
+        st_e4m3_stream<TL::VEC>(static_cast<uint8_t*>(rc) + off, scale, t);
+    }
+}
+
+// ------------------------------------------------------------------ warp reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, off));
+  return v;
+}
+
+// Sum M per-lane values over the 32 lanes at once ("transpose reduction"): each halving
+// step trades half of the values with the lane `off` away, so M sums cost
+// M-1 + log2(32/M) shuffles instead of 5M. Lane l ends with the sum of value
+// transpose_index<M>(l); the lanes with (l & (32/M - 1)) == 0 hold distinct values.
+template <int M>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[M], int lane) {
+  static_assert(M >= 1 && M <= 32 && (M & (M - 1)) == 0, "M must be a power of two <= 32");
+#pragma unroll
+  for (int w = M / 2, off = 16; w >= 1; w >>= 1, off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = up ? v[i] : v[i + w];
+      const float keep = up ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFull, send, off);
+    }
+  }
+  float s = v[0];
+#pragma unroll
+  for (int off = 16 / M; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  return s;
+}
+template <int M>
+__device__ __forceinline__ int transpose_index(int lane) {
+  int idx = 0;
+#pragma unroll
+  for (int w = M / 2, off = 16; w >= 1; w >>= 1, off >>= 1)
+    if (lane & off) idx += w;
+  return idx;
+}
+template <int M>
+__device__ __forceinline__ bool transpose_leader(int lane) {
+  return (lane & (32 / M - 1)) == 0;
+}
+
+// ------------------------------------------------------------------ small helpers
+// Load RPW consecutive elements of one record row (rows w*RPW.. of an x vector).
+template <int RPW, class T>
+__device__ __forceinline__ void load_rows(const T* p, float (&o)[RPW]) {
+#pragma unroll
+  for (int i = 0; i < RPW; i += 4) {
+    float t[4];
+    ldv<4>(p + i, t);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[i + e] = t[e];
+  }
+}
+
+__device__ __forceinline__ int ring_slot(int start, int s, int cap) {
+  int v = start + s;
+  return v >= cap ? v - cap : v;
+}
+
+__device__ __forceinline__ void set_status(int* status, int bit) { atomicOr(status, bit); }
+
+// Last-CTA-done update of a sequence's metadata: every CTA of sequence b calls this once,
+// after its single reader thread has read meta[b]; the last of the H arrivals writes the
+// new value and re-arms the counter. Nothing waits, so nothing can hang.
+__device__ __forceinline__ void arrive_and_publish(const StoreView& sv, int b, int4 next) {
+  __threadfence();
+  const int old = atomicAdd(&sv.arrive[b], 1);
+  if (old == sv.H - 1) {
+    sv.arrive[b] = 0;
+    sv.meta[b] = next;
+  }
+}
+
+}  // namespace rssm

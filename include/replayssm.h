@@ -1,0 +1,203 @@
+/*
+ * replayssm.h -- C ABI of the ReplaySSM decode library for one Mamba-2 layer (sm_103a).
+ *
+ * Source of the method: the NVIDIA Developer blog post "ReplaySSM: Rethinking State
+ * Storage for Faster Hybrid-Model Decoding". Each call below names the section of that
+ * page that defines the operation. The page's displayed formulas were lost; the
+ * operation is stated here in full.
+ *
+ * Model (per sequence b and head h; head h reads group g = h / (H/G)):
+ *     a_t = exp(dt_t * A_h)
+ *     h_t = a_t * h_{t-1} + dt_t * x_t B_t^T          (P x N state)
+ *     y_t = h_t C_t + D_h * x_t
+ * ("Why SSM layers can become a decoding bottleneck".) ReplaySSM keeps h as an FP32
+ * checkpoint h0 plus a ring of the input records (x_s, B_s, dt_s) appended since the
+ * checkpoint ("How ReplaySSM represents the state"). With the n records numbered
+ * s = 1..k (k = n + 1 including the current token):
+ *     y_k = Gamma_k (h0 C_k) + sum_s gamma(k,s) dt_s (B_s . C_k) x_s + D x_k
+ *     gamma(k,s) = exp(A sum_{r=s+1..k} dt_r),  Gamma_k = exp(A sum_{r=1..k} dt_r)
+ *
+ * Conventions for every call:
+ *  - Ownership: all device memory (workspace, inputs, outputs, A, D) belongs to the
+ *    caller and is passed as plain device pointers. The library owns only the small
+ *    host handle returned by replay_alloc. It allocates no device memory.
+ *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *    device call is asynchronous on that stream and launches on no other stream.
+ *  - Return codes: REPLAY_OK, or a negative REPLAY_E* code for errors found on the host
+ *    (nothing is launched then). Errors found on the device never trap: they set bits of
+ *    the store's status word (REPLAY_DEV_*), read with replay_status.
+ *  - Layouts: dense, row-major, last index fastest:
+ *      x [batch][H][P], B and C [batch][G][N], dt [batch][H], y [batch][H][P]  (one token)
+ *      x [batch][T][H][P], B and C [batch][T][G][N], dt [batch][T][H],
+ *      y [batch][T][H][P]                                                     (T drafts)
+ *      A, D [H] FP32 on the device; states [batch][H][P][N] FP32.
+ *    x, B, C and dt are FP32 or bf16 (replay_config.in_dtype); y is always FP32.
+ *  - Supported shapes: headdim P = 64 and dstate N in {64, 128, 256}; H a multiple of G;
+ *    ring capacity (see replay_layout) at most 64 records.
+ */
+#ifndef REPLAYSSM_H
+#define REPLAYSSM_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define REPLAY_ABI_VERSION 1
+
+/* element types of x, B, C, dt and of the ring records */
+#define REPLAY_F32 0
+#define REPLAY_BF16 1
+
+/* low-precision read copy of the checkpoint */
+#define REPLAY_RC_NONE 0
+#define REPLAY_RC_BF16 1     /* bf16, round to nearest even */
+#define REPLAY_RC_FP8E4M3 2  /* OCP E4M3, RNE, saturating; FP32 scale absmax/448 per (b, h) */
+
+/* host return codes */
+#define REPLAY_OK 0
+#define REPLAY_EBADARG (-1)      /* null pointer, bad count, store/shape mismatch */
+#define REPLAY_EUNSUPPORTED (-2) /* shape or dtype this build has no kernel for */
+#define REPLAY_ECAPACITY (-3)    /* ring capacity or draft count beyond the configured maximum */
+#define REPLAY_ECUDA (-4)        /* a CUDA call or launch failed */
+
+/* device status bits (sticky until cleared by replay_status or replay_reset) */
+#define REPLAY_DEV_BAD_META 1    /* a sequence's ring metadata was out of range: its y is NaN */
+#define REPLAY_DEV_BAD_ACCEPT 2  /* commit with accept < 0 or > drafts pending: not applied */
+
+typedef struct replay_config {
+  int batch;        /* sequences */
+  int nheads;       /* H */
+  int headdim;      /* P */
+  int dstate;       /* N */
+  int ngroups;      /* G: B and C are shared by the H/G heads of a group */
+  int window_L;     /* records folded per flush (the window) */
+  int max_draft_T;  /* largest T passed to replay_verify; 0 = no speculative verify */
+  int in_dtype;     /* REPLAY_F32 or REPLAY_BF16 */
+  int read_copy;    /* REPLAY_RC_* */
+} replay_config;
+
+/* Byte offsets of the regions inside the caller's workspace (each 256-byte aligned).
+ *   h0     FP32 checkpoint            [batch][H][P][N]
+ *   rc     read copy (bf16 or E4M3)   [batch][H][P][N]      (0 bytes without a copy)
+ *   scale  FP32 E4M3 scale            [batch][H]            (0 bytes unless E4M3)
+ *   xbuf   ring of x records          [batch][H][cap][P]    (in_dtype)
+ *   bbuf   ring of B records          [batch][G][cap][N]    (in_dtype)
+ *   dtbuf  ring of dt records         [batch][H][cap]       (in_dtype)
+ *   meta   per sequence int32 x4      {start, n, pending, 0}: records live in ring slots
+ *          (start + s) mod cap, s < n; `pending` drafts sit beyond them after a verify
+ *   arrive per sequence int32 counter (internal; zero between calls)
+ *   status int32 device status word (REPLAY_DEV_* bits)
+ * cap = window_L when max_draft_T == 0, else window_L + 2*max_draft_T - 1: the most
+ * records a sequence can hold (window_L - 1 + T committed before a verify folds them)
+ * plus T drafts written beyond them while those are being folded. */
+typedef struct replay_layout {
+  size_t h0, rc, scale, xbuf, bbuf, dtbuf, meta, arrive, status;
+  size_t total;  /* workspace bytes */
+  int cap;       /* ring capacity in records */
+} replay_layout;
+
+typedef struct replay_store replay_store; /* opaque host handle */
+
+/* Validate a config and compute its workspace layout. No CUDA call. */
+int replay_layout_of(const replay_config* cfg, replay_layout* out);
+
+/* Workspace bytes the caller must allocate for cfg. No CUDA call. */
+int replay_store_bytes(const replay_config* cfg, size_t* bytes);
+
+/* Bind a store to a caller-owned device workspace of at least replay_store_bytes bytes
+ * (256-byte aligned) and to the per-head A (< 0) and D vectors, which must stay valid
+ * while the store is used. Launches a reset on `stream`: h0 = 0 and every ring empty.
+ * The handle is freed with replay_free. */
+int replay_alloc(const replay_config* cfg, void* workspace, size_t workspace_bytes,
+                 const float* A, const float* D, void* stream, replay_store** out);
+
+/* Free the host handle. The workspace stays the caller's. */
+int replay_free(replay_store* st);
+
+/* Reset sequences: h0 = 0, ring emptied, pending drafts dropped. seq_mask is a device
+ * int32 [batch] (nonzero = reset) or NULL for all sequences; with NULL the status word is
+ * cleared as well. */
+int replay_reset(replay_store* st, const int* seq_mask, void* stream);
+
+/* Import a state for every sequence: h0 = h (FP32 [batch][H][P][N], device), rings
+ * emptied, and the read copy recast from h. Used to resume, or to hand over a state
+ * computed elsewhere (e.g. by prefill). */
+int replay_load_state(replay_store* st, const float* h, void* stream);
+
+/* Write the current state of every sequence -- h0 with the committed records folded in
+ * (the unrolled window of "How ReplaySSM represents the state") -- to h_out (FP32
+ * [batch][H][P][N], device). The store is not modified. */
+int replay_export_state(replay_store* st, float* h_out, void* stream);
+
+/* One decode token for every sequence ("How ReplaySSM represents the state";
+ * "Benefit 1: Reduce state memory traffic"). With k = n + 1:
+ *  - k < window_L (non-flush step): y from checkpoint + records + the current inputs;
+ *    the record (x, B, dt) is appended to the ring; no state is written.
+ *  - k >= window_L (flush step): the k records (this token's included) are folded into
+ *    h0, which is written once (and cast into the read copy, if any); y is read from the
+ *    new FP32 checkpoint; the ring is emptied.
+ * Non-flush steps read the read copy when one is configured; flushes always start from
+ * the FP32 checkpoint ("Benefit 3"). Drafts pending from a verify are dropped. */
+int replay_step(replay_store* st, const void* x, const void* B, const void* C,
+                const void* dt, float* y, void* stream);
+
+/* Speculative verify of T drafts (1 <= T <= max_draft_T) for every sequence ("Benefit 2:
+ * Simplify rollback and speed up verification"). If the sequence holds n >= window_L
+ * committed records they are folded into h0 first (a flush of committed records only).
+ * Then y[b][j] (j = 0..T-1) is the output the model would give after decoding drafts
+ * 0..j in order, computed from checkpoint + committed records + drafts without forming a
+ * state. The drafts' records are written to the ring beyond the committed ones; the
+ * commit pointer does not move until replay_commit. */
+int replay_verify(replay_store* st, int T, const void* x, const void* B, const void* C,
+                  const void* dt, float* y, void* stream);
+
+/* Commit the first accept[b] drafts of the last verify of each sequence (device int32
+ * [batch], 0 <= accept[b] <= T): the ring pointer advances over them; the other drafts are
+ * left beyond the pointer, ignored, and overwritten by the next append ("Benefit 2").
+ * Nothing is restored. An out-of-range accept sets REPLAY_DEV_BAD_ACCEPT and commits
+ * nothing for that sequence. */
+int replay_commit(replay_store* st, const int* accept, void* stream);
+
+/* Fold every sequence's committed records into h0 now (n > 0), writing h0 (and the read
+ * copy) once and emptying the ring; pending drafts are dropped. */
+int replay_flush(replay_store* st, void* stream);
+
+/* Copy the device status word to *status_out (host), synchronising `stream`; clear it
+ * afterwards if `clear` is nonzero. */
+int replay_status(replay_store* st, int* status_out, int clear, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Conventional baselines ("Why SSM layers can become a decoding bottleneck"; "Rollback
+ * for speculative decoding"). They use the config's shape fields and in_dtype only.
+ * --------------------------------------------------------------------------------- */
+
+/* Load-update-store decode step: state <- a * state + dt x B^T, y = state C + D x, state
+ * stored back. state is [batch][H][P][N], FP32 (state_dtype REPLAY_F32) or bf16
+ * (REPLAY_BF16: FP32 arithmetic, stored with round-to-nearest-even). */
+int conv_step(const replay_config* cfg, void* state, int state_dtype, const float* A,
+              const float* D, const void* x, const void* B, const void* C, const void* dt,
+              float* y, void* stream);
+
+/* Snapshot-per-draft verify: one read of snapshot slot cur[b], T updates, snapshot j
+ * (after draft j) written to slot (cur[b] + 1 + j) mod (T + 1), outputs y[b][j].
+ * snaps is FP32 [batch][T+1][H][P][N]; cur is device int32 [batch]. */
+int conv_verify_snapshot(const replay_config* cfg, int T, float* snaps, const int* cur,
+                         const float* A, const float* D, const void* x, const void* B,
+                         const void* C, const void* dt, float* y, void* stream);
+
+/* Pick the snapshot of the accepted prefix: cur[b] <- (cur[b] + accept[b]) mod (T + 1).
+ * An accept outside 0..T leaves cur[b] and sets bit REPLAY_DEV_BAD_ACCEPT of *status
+ * (device int32, may be NULL). */
+int conv_commit(int batch, int T, int* cur, const int* accept, int* status, void* stream);
+
+/* Text for a return code; library version. */
+const char* replay_strerror(int code);
+int replay_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REPLAYSSM_H */

@@ -1,0 +1,69 @@
+"""The C ABI library on the host (no GPU needed): it loads, exports every declared
+symbol, computes layouts, and rejects bad arguments before any CUDA call."""
+import ctypes
+
+import pytest
+
+from hybrid_model_ssm_mamba_gb300 import replay as R
+
+
+def test_exports_every_header_symbol(lib):
+    names = R.header_functions()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.replay_abi_version() == 1
+    assert lib.replay_strerror(-3) == b"capacity exceeded"
+
+
+def test_layout_of_nemotron_layer():
+    cfg = R.ReplayConfig(256, 128, 64, 128, 8, 16, 0, R.REPLAY_BF16, R.REPLAY_RC_NONE)
+    L = R.replay_layout_of(cfg)
+    assert L.cap == 16
+    assert L.h0 == 0 and L.rc == 1 << 30 and L.xbuf == 1 << 30
+    assert L.bbuf - L.xbuf == 256 * 128 * 16 * 64 * 2
+    assert L.dtbuf - L.bbuf == 256 * 8 * 16 * 128 * 2
+    for name in ("h0", "rc", "scale", "xbuf", "bbuf", "dtbuf", "meta", "arrive", "status", "total"):
+        assert getattr(L, name) % 256 == 0
+    assert R.replay_store_bytes(cfg) == L.total
+
+
+def test_layout_ring_capacity_and_read_copies():
+    cfg = R.ReplayConfig(512, 8, 64, 128, 1, 16, 4, R.REPLAY_F32, R.REPLAY_RC_FP8E4M3)
+    L = R.replay_layout_of(cfg)
+    assert L.cap == 16 + 2 * 4 - 1
+    assert L.scale - L.rc == 512 * 8 * 64 * 128
+    assert L.xbuf - L.scale == 512 * 8 * 4
+    cfg.read_copy = R.REPLAY_RC_BF16
+    L = R.replay_layout_of(cfg)
+    assert L.scale - L.rc == 512 * 8 * 64 * 128 * 2 and L.xbuf == L.scale
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("batch", 0, -1), ("nheads", 6, -1), ("ngroups", 0, -1), ("window_L", 0, -1),
+    ("max_draft_T", -1, -1), ("in_dtype", 7, -1), ("read_copy", 3, -1), ("headdim", 48, -2),
+    ("dstate", 96, -2), ("window_L", 65, -3), ("max_draft_T", 9, -3)])
+def test_layout_rejects(field, value, code):
+    cfg = R.ReplayConfig(4, 8, 64, 128, 4, 16, 2, R.REPLAY_F32, R.REPLAY_RC_NONE)
+    setattr(cfg, field, value)
+    with pytest.raises(R.ReplayError) as e:
+        R.replay_layout_of(cfg)
+    assert e.value.code == code
+
+
+def test_calls_reject_null_arguments_before_cuda(lib):
+    cfg = R.ReplayConfig(4, 8, 64, 128, 4, 16, 2, R.REPLAY_F32, R.REPLAY_RC_NONE)
+    out = ctypes.c_void_p()
+    assert lib.replay_alloc(ctypes.byref(cfg), None, 1 << 20, None, None, None, ctypes.byref(out)) == -1
+    assert lib.replay_alloc(ctypes.byref(cfg), 256, 16, 256, 256, None, ctypes.byref(out)) == -3
+    assert lib.replay_alloc(ctypes.byref(cfg), 255, 1 << 40, 256, 256, None, ctypes.byref(out)) == -1
+    assert lib.replay_step(None, 256, 256, 256, 256, 256, None) == -1
+    assert lib.replay_verify(None, 2, 256, 256, 256, 256, 256, None) == -1
+    assert lib.replay_commit(None, 256, None) == -1
+    assert lib.replay_flush(None, None) == -1
+    assert lib.replay_free(None) == -1
+    assert lib.conv_step(ctypes.byref(cfg), None, 0, 256, 256, 256, 256, 256, 256, 256, None) == -1
+    assert lib.conv_step(ctypes.byref(cfg), 256, 5, 256, 256, 256, 256, 256, 256, 256, None) == -1
+    assert lib.conv_commit(4, 0, 256, 256, None, None) == -1
+    bad = R.ReplayConfig(4, 8, 64, 96, 4, 16, 2, R.REPLAY_F32, R.REPLAY_RC_NONE)
+    assert lib.conv_step(ctypes.byref(bad), 256, 0, 256, 256, 256, 256, 256, 256, 256, None) == -2

@@ -1,0 +1,294 @@
+"""GPU parity of the replay path against the FP64 oracle, through the C ABI.
+
+Bar (FP32 path): every output vector and every checkpoint slab within 1e-4 relative
+(inf-norm per vector, see gpu_util); bf16 read copy within 1e-2; integer metadata exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthgen as sg
+from gpu_util import DTYPE, draft_device, make_store, rel_vec_err, step_inputs
+from hybrid_model_ssm_mamba_gb300 import replay as R
+from oracle import formats as F
+from oracle.mamba2 import Mamba2Decoder
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def run_decode(shape, steps, L, seed=0, read_copy=R.REPLAY_RC_NONE, seqs=None, check_ckpt=True,
+               on_step=None):
+    """Decode `steps` tokens on the GPU and in the oracle (sequences `seqs`); returns the
+    worst output error, the worst post-flush checkpoint error and the store."""
+    st, A, D = make_store(shape, seed, L=L, read_copy=read_copy)
+    sel = np.arange(shape.batch) if seqs is None else np.asarray(seqs)
+    H, P, N = shape.nheads, shape.headdim, shape.dstate
+    orc = Mamba2Decoder(A, D, shape.ngroups, np.zeros((len(sel), H, P, N)))
+    y = torch.empty(shape.batch, H, P, device="cuda")
+    worst_y = worst_h = 0.0
+    for t in range(steps):
+        devs, f64 = step_inputs(shape, seed, t, sel)
+        st.step(*devs, y)
+        yref = orc.step(*f64)
+        worst_y = max(worst_y, rel_vec_err(y[sel].cpu().numpy(), yref, 2).max())
+        if check_ckpt and (t + 1) % L == 0:
+            h0 = st.region("h0")[sel].cpu().numpy()
+            worst_h = max(worst_h, rel_vec_err(h0, orc.h, 2).max())
+        if on_step is not None:
+            on_step(t, st, orc)
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    return worst_y, worst_h, st, orc
+
+
+def test_tiny_layer_all_steps():
+    """Tiny Mamba-2 layer: batch 1, 8 heads, P 64, N 128, G 1, FP32, L 16, 64 steps."""
+    shape = sg.LayerShape(1, 8, 64, 128, 1, "f32")
+    wy, wh, st, orc = run_decode(shape, 64, 16)
+    assert wy <= TOL and wh <= TOL, (wy, wh)
+    meta = st.region("meta").cpu().numpy()
+    assert meta[0, 1] == 0 and meta[0, 2] == 0           # 64 = 4 windows: ring empty
+
+
+@pytest.mark.parametrize("N,dtype,G,L,steps", [
+    (128, "bf16", 2, 5, 13), (64, "f32", 3, 7, 17), (256, "bf16", 1, 4, 9), (128, "f32", 6, 1, 5),
+    (128, "f32", 2, 40, 45)])
+def test_ragged_shapes(N, dtype, G, L, steps):
+    """Odd batch and head counts, several group sizes, windows that do not divide the run."""
+    shape = sg.LayerShape(3, 6, 64, N, G, dtype)
+    wy, wh, st, orc = run_decode(shape, steps, L, seed=3)
+    assert wy <= TOL and wh <= TOL, (wy, wh)
+    meta = st.region("meta").cpu().numpy()
+    assert np.all(meta[:, 1] == steps % L)
+    assert np.all(meta[:, 0] == (steps - steps % L) % L)
+    h = torch.empty(3, 6, 64, N, device="cuda")
+    st.export_state(h)
+    assert rel_vec_err(h.cpu().numpy(), orc.h, 2).max() <= TOL
+
+
+def test_export_does_not_mutate_and_load_roundtrips():
+    shape = sg.LayerShape(2, 4, 64, 128, 2, "f32")
+    st, A, D = make_store(shape, 1, L=8)
+    h0 = torch.from_numpy(sg.initial_state(shape, 1)).cuda()
+    st.load_state(h0)
+    out = torch.empty_like(h0)
+    st.export_state(out)
+    assert torch.equal(out, h0)
+    orc = Mamba2Decoder(A, D, 2, h0.cpu().numpy().astype(np.float64))
+    y = torch.empty(2, 4, 64, device="cuda")
+    for t in range(11):
+        devs, f64 = step_inputs(shape, 1, t)
+        st.step(*devs, y)
+        assert rel_vec_err(y.cpu().numpy(), orc.step(*f64), 2).max() <= TOL
+    meta_before = st.region("meta").clone()
+    h0_before = st.region("h0").clone()
+    st.export_state(out)
+    st.export_state(out)
+    assert torch.equal(st.region("meta"), meta_before) and torch.equal(st.region("h0"), h0_before)
+    assert rel_vec_err(out.cpu().numpy(), orc.h, 2).max() <= TOL
+
+
+def test_forced_flush_and_staggered_phases():
+    """replay_flush mid-window, and per-sequence resets that leave sequences in different
+    phases within one launch."""
+    shape = sg.LayerShape(4, 4, 64, 128, 1, "bf16")
+    st, A, D = make_store(shape, 2, L=6)
+    orc = Mamba2Decoder(A, D, 1, np.zeros((4, 4, 64, 128)))
+    y = torch.empty(4, 4, 64, device="cuda")
+    for t in range(23):
+        devs, f64 = step_inputs(shape, 2, t)
+        if t == 4:
+            st.flush()
+            assert st.region("meta").cpu().numpy()[:, 1].tolist() == [0, 0, 0, 0]
+        if t in (7, 15):
+            mask = torch.tensor([0, 1, 0, 1] if t == 7 else [1, 0, 0, 0], dtype=torch.int32, device="cuda")
+            st.reset(mask)
+            orc.h[mask.cpu().numpy().astype(bool)] = 0.0
+        st.step(*devs, y)
+        assert rel_vec_err(y.cpu().numpy(), orc.step(*f64), 2).max() <= TOL, t
+    n = st.region("meta").cpu().numpy()[:, 1]
+    assert len(set(n.tolist())) > 1          # the sequences really are out of phase
+    assert st.status() == 0
+
+
+@pytest.mark.parametrize("L", [1, 4, 8, 16, 32])
+def test_window_length_invariance(L):
+    """Outputs do not depend on the window; L = 1 is the conventional step."""
+    shape = sg.LayerShape(2, 8, 64, 128, 2, "f32")
+    wy, wh, _, _ = run_decode(shape, 40, L, seed=5)
+    assert wy <= TOL and wh <= TOL, (L, wy, wh)
+
+
+def test_replay_equals_conventional_gpu():
+    """GPU replay == GPU load-update-store on the same inputs (bf16 inputs, FP32 state)."""
+    shape = sg.LayerShape(4, 16, 64, 128, 4, "bf16")
+    st, A, D = make_store(shape, 6, L=16)
+    cfg = st.cfg
+    state = torch.zeros(4, 16, 64, 128, device="cuda")
+    y1 = torch.empty(4, 16, 64, device="cuda")
+    y2 = torch.empty_like(y1)
+    for t in range(35):
+        devs, _ = step_inputs(shape, 6, t)
+        st.step(*devs, y1)
+        R.conv_step(cfg, state, R.REPLAY_F32, st.A, st.D, *devs, y2)
+        assert rel_vec_err(y1.cpu().numpy(), y2.cpu().numpy(), 2).max() <= TOL, t
+    h = torch.empty_like(state)
+    st.export_state(h)
+    assert rel_vec_err(h.cpu().numpy(), state.cpu().numpy(), 2).max() <= TOL
+
+
+def test_nemotron_layer_sampled_sequences():
+    """Nemotron-shaped layer at full size (batch 256, 128 heads, G 8, bf16 inputs, L 16,
+    256 steps = 16 flushes), in the launch configuration the benchmark times; the oracle
+    follows four seeded sequences (all heads, every step and every checkpoint)."""
+    shape = sg.LayerShape(256, 128, 64, 128, 8, "bf16")
+    seqs = np.sort(np.random.default_rng(0).choice(256, 4, replace=False))
+    wy, wh, st, _ = run_decode(shape, 256, 16, seed=0, seqs=seqs)
+    assert wy <= TOL and wh <= TOL, (wy, wh)
+    meta = st.region("meta").cpu().numpy()
+    assert np.all(meta[:, 1] == 0) and np.all(meta[:, 0] == 0)
+
+
+def test_read_copy_bf16_bound():
+    """bf16 read copy: non-flush outputs within 1e-2 of the FP64 oracle."""
+    shape = sg.LayerShape(8, 8, 64, 128, 1, "f32")
+    wy, wh, _, _ = run_decode(shape, 48, 16, seed=7, read_copy=R.REPLAY_RC_BF16)
+    assert wy <= 1e-2 and wh <= TOL, (wy, wh)
+
+
+def test_read_copy_fp8_drift_is_bounded():
+    """E4M3 read copy: drift is reported, not bounded by the pages; check it stays an
+    E4M3-sized read error (no growth) and the FP32 checkpoints stay exact."""
+    shape = sg.LayerShape(8, 8, 64, 128, 1, "f32")
+    wy, wh, _, _ = run_decode(shape, 64, 16, seed=8, read_copy=R.REPLAY_RC_FP8E4M3)
+    assert wh <= TOL and wy <= 0.25, (wy, wh)
+
+
+@pytest.mark.parametrize("rc", [R.REPLAY_RC_BF16, R.REPLAY_RC_FP8E4M3])
+def test_read_copy_codes_match_format_definitions(rc):
+    """The copy written by a checkpoint write equals the format encoders applied to the
+    same FP32 state, bit for bit (codes decided in FP32 on both sides)."""
+    shape = sg.LayerShape(3, 4, 64, 128, 1, "f32")
+    st, _, _ = make_store(shape, 9, L=4, read_copy=rc)
+    h = sg.initial_state(shape, 9)
+    h[0, 1] = 0.0                                  # an all-zero slab: scale 1
+    h[1, 2, 0, :4] = [1e-12, -3e-9, 500.0, -1e30]  # tiny, subnormal-range and huge values
+    st.load_state(torch.from_numpy(h).cuda())
+    got = st.region("rc").cpu()
+    if rc == R.REPLAY_RC_BF16:
+        assert np.array_equal(got.view(torch.int16).numpy().view(np.uint16), F.bf16_encode(h))
+    else:
+        scale = st.region("scale").cpu().numpy()
+        for b in range(3):
+            for hh in range(4):
+                q, s = F.fp8_slab_quantize(h[b, hh])
+                assert np.float32(scale[b, hh]) == s
+                g = got.numpy()[b, hh]
+                same = (g == q) | ((g & 0x7F) == 0) & ((q & 0x7F) == 0)   # +-0 both zero
+                assert same.all(), (b, hh, np.argwhere(~same)[:3])
+
+
+def test_verify_commit_matches_oracle():
+    """Speculative verify + commit with accept ~ U{0..T}, interleaved with decode steps:
+    every verify output and the final state match an oracle that decodes only the
+    accepted prefixes."""
+    shape = sg.LayerShape(8, 8, 64, 128, 2, "f32")
+    T, L = 4, 8
+    st, A, D = make_store(shape, 11, L=L, T=T)
+    orc = Mamba2Decoder(A, D, 2, np.zeros((8, 8, 64, 128)))
+    y = torch.empty(8, T, 8, 64, device="cuda")
+    y1 = torch.empty(8, 8, 64, device="cuda")
+    worst = 0.0
+    for call in range(24):
+        if call % 5 == 4:
+            devs, f64 = step_inputs(shape, 11, 1000 + call)
+            st.step(*devs, y1)
+            worst = max(worst, rel_vec_err(y1.cpu().numpy(), orc.step(*f64), 2).max())
+        devs, f64 = draft_device(shape, 11, call, T)
+        st.verify(T, *devs, y)
+        worst = max(worst, rel_vec_err(y.cpu().numpy(), orc.verify(*f64), 3).max())
+        acc = sg.accept_lengths(8, T, 11, call)
+        if call == 3:
+            acc[:] = 0
+        if call == 6:
+            acc[:] = T
+        st.commit(torch.from_numpy(acc).cuda())
+        orc.commit(acc, f64[0], f64[1], f64[3])
+        meta = st.region("meta").cpu().numpy()
+        assert np.all(meta[:, 1] <= L - 1 + T) and np.all(meta[:, 2] == 0)
+    assert worst <= TOL, worst
+    h = torch.empty(8, 8, 64, 128, device="cuda")
+    st.export_state(h)
+    assert rel_vec_err(h.cpu().numpy(), orc.h, 2).max() <= TOL
+    assert st.status() == 0
+
+
+@pytest.mark.parametrize("rc", [R.REPLAY_RC_NONE, R.REPLAY_RC_BF16])
+def test_verify_workload_shape(rc):
+    """The speculative workload's shape (batch 512, 8 heads, T 4, ring of 23), 20 verify
+    calls; the oracle follows 6 seeded sequences."""
+    shape = sg.LayerShape(512, 8, 64, 128, 1, "f32")
+    T, L = 4, 16
+    st, A, D = make_store(shape, 12, L=L, T=T, read_copy=rc)
+    assert st.layout.cap == 23
+    sel = np.array([0, 77, 200, 311, 480, 511])
+    orc = Mamba2Decoder(A, D, 1, np.zeros((6, 8, 64, 128)))
+    y = torch.empty(512, T, 8, 64, device="cuda")
+    worst = 0.0
+    for call in range(20):
+        devs, f64 = draft_device(shape, 12, call, T)
+        st.verify(T, *devs, y)
+        f64s = [a[sel] for a in f64]
+        worst = max(worst, rel_vec_err(y[sel].cpu().numpy(), orc.verify(*f64s), 3).max())
+        acc = sg.accept_lengths(512, T, 12, call)
+        st.commit(torch.from_numpy(acc).cuda())
+        orc.commit(acc[sel], f64s[0], f64s[1], f64s[3])
+    bound = TOL if rc == R.REPLAY_RC_NONE else 1e-2
+    assert worst <= bound, worst
+    assert st.status() == 0
+
+
+def test_bad_accept_sets_status_and_commits_nothing():
+    shape = sg.LayerShape(2, 2, 64, 128, 1, "f32")
+    st, _, _ = make_store(shape, 13, L=4, T=2)
+    devs, _ = draft_device(shape, 13, 0, 2)
+    y = torch.empty(2, 2, 2, 64, device="cuda")
+    st.verify(2, *devs, y)
+    st.commit(torch.tensor([3, 1], dtype=torch.int32, device="cuda"))
+    meta = st.region("meta").cpu().numpy()
+    assert meta[0, 1] == 0 and meta[1, 1] == 1 and np.all(meta[:, 2] == 0)
+    assert st.status(clear=True) == R.REPLAY_DEV_BAD_ACCEPT
+    assert st.status() == 0
+    st.commit(torch.tensor([1, 0], dtype=torch.int32, device="cuda"))   # nothing pending
+    assert st.status() == R.REPLAY_DEV_BAD_ACCEPT
+
+
+def test_corrupt_metadata_gives_nan_and_status():
+    shape = sg.LayerShape(2, 2, 64, 128, 1, "f32")
+    st, _, _ = make_store(shape, 14, L=4)
+    st.region("meta")[1, 1] = 99                        # beyond the ring
+    devs, _ = step_inputs(shape, 14, 0)
+    y = torch.zeros(2, 2, 64, device="cuda")
+    st.step(*devs, y)
+    assert st.status() & R.REPLAY_DEV_BAD_META
+    assert torch.isnan(y[1]).all() and not torch.isnan(y[0]).any()
+
+
+def test_host_errors():
+    shape = sg.LayerShape(2, 2, 64, 128, 1, "f32")
+    st, _, _ = make_store(shape, 15, L=4, T=2)
+    devs, _ = draft_device(shape, 15, 0, 2)
+    y = torch.empty(2, 3, 2, 64, device="cuda")
+    with pytest.raises(R.ReplayError) as e:
+        st.verify(3, *devs, y)
+    assert e.value.code == -3
+    with pytest.raises(R.ReplayError) as e:
+        st.verify(0, *devs, y)
+    assert e.value.code == -1
