@@ -291,6 +291,11 @@ def run_replay(args, rank, world, local_rank):
     torch.cuda.synchronize()
     conv_s = c0.elapsed_time(c1) / 1e3 / (c_steps * L)
     conv_tps = w["batch"] / conv_s
+    del state
+    extra = {}
+    if not args.no_extra:
+        extra["read_copy"] = run_read_copies(torch, R, dev)
+        extra["speculative"] = run_speculative(torch, R)
 
     result = {
         "metric": METRIC, "value": tokens / elapsed_max, "unit": UNIT, "n_gpus": world,
@@ -309,7 +314,9 @@ def run_replay(args, rank, world, local_rank):
                      "kernel": "replay_step_kernel (window average)",
                      "algorithmic_bytes_per_launch": alg_bytes / (args.steps * L),
                      "nonflush_achieved": nf_bytes / nf_s / 1e9,
-                     "nonflush_frac": nf_bytes / nf_s / 1e9 / peak},
+                     "nonflush_frac": nf_bytes / nf_s / 1e9 / peak,
+                     "nonflush_launch_us": float(launch_s[:, :-1].mean() * 1e6),
+                     "flush_launch_us": float(launch_s[:, -1].mean() * 1e6)},
         "e2e": {"value": world * w["batch"] * L * e_steps / e_el, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * L,
@@ -317,6 +324,7 @@ def run_replay(args, rank, world, local_rank):
                       "conv_step_achieved_gbs": conv_bytes(w) / conv_s / 1e9,
                       "replay_speedup_vs_conv": (w["batch"] * L * args.steps / elapsed) / conv_tps},
         "clocks": clk.summary(),
+        "extra": extra,
     }
     if rank == 0:
         result["cpu_baseline"] = cpu_baseline(args.cpu_sample_seqs, args.cpu_sample_tokens)
@@ -325,6 +333,112 @@ def run_replay(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.destroy_process_group()
     return result if rank == 0 else None
+
+
+# ------------------------------------------------------------------ secondary workloads
+SPEC = dict(batch=512, nheads=8, headdim=64, dstate=128, ngroups=1, dtype="f32", L=16, T=4)
+
+
+def l2_flusher(torch):
+    """A buffer at least twice the L2 size; writing it evicts earlier data from L2."""
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    buf = torch.empty(max(2 * l2, 1 << 28) // 4, dtype=torch.float32, device="cuda")
+    return lambda: buf.fill_(1.0)
+
+
+def run_speculative(torch, R, calls=64, distinct=16):
+    """Speculative verify on the tiny layer's shape at batch 512, T = 4, accept ~ U{0..T}:
+    ReplaySSM verify + commit against snapshot-per-draft verify + commit, and against one
+    conventional decode step of the same shape; L2 is flushed before every timed call."""
+    w = SPEC
+    T, L = w["T"], w["L"]
+    shape = sg.LayerShape(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["dtype"])
+    A, D = sg.head_params(w["nheads"], 0)
+    cfg = R.ReplayConfig(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], L, T,
+                         R.REPLAY_F32, R.REPLAY_RC_NONE)
+    st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
+    drafts = []
+    for c in range(distinct):
+        d = sg.draft_inputs(shape, 0, c, T)
+        drafts.append([torch.from_numpy(d[k].store).cuda() for k in ("x", "B", "C", "dt")])
+    accepts = [torch.from_numpy(sg.accept_lengths(w["batch"], T, 0, c)).cuda() for c in range(calls)]
+    y = torch.empty(w["batch"], T, w["nheads"], w["headdim"], device="cuda")
+    snaps = torch.zeros(w["batch"], T + 1, w["nheads"], w["headdim"], w["dstate"], device="cuda")
+    cur = torch.zeros(w["batch"], dtype=torch.int32, device="cuda")
+    state = torch.zeros(w["batch"], w["nheads"], w["headdim"], w["dstate"], device="cuda")
+    y1 = torch.empty(w["batch"], w["nheads"], w["headdim"], device="cuda")
+    first = [[t[:, 0].contiguous() for t in dr] for dr in drafts]
+    flush = l2_flusher(torch)
+
+    def timed(fn):
+        ts = []
+        for c in range(calls):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn(c)
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in ts])) * 1e3
+
+    def replay(c):
+        st.verify(T, *drafts[c % distinct], y)
+        st.commit(accepts[c])
+
+    def snapshot(c):
+        R.conv_verify_snapshot(cfg, T, snaps, cur, st.A, st.D, *drafts[c % distinct], y)
+        R.conv_commit(w["batch"], T, cur, accepts[c])
+
+    def standard(c):
+        R.conv_step(cfg, state, R.REPLAY_F32, st.A, st.D, *first[c % distinct], y1)
+
+    for fn in (replay, snapshot, standard):
+        fn(0)
+    r_us, s_us, c_us = timed(replay), timed(snapshot), timed(standard)
+    assert st.status() == 0
+    st.close()
+    return {"workload": "tiny-layer shape at batch 512, 8 heads, T=4, accept ~ U{0..4}, L2 flushed per call",
+            "replay_verify_commit_us": r_us, "snapshot_verify_commit_us": s_us,
+            "conventional_step_us": c_us, "replay_speedup_vs_snapshot": s_us / r_us,
+            "snapshot_vs_standard_step": s_us / c_us, "replay_vs_standard_step": r_us / c_us,
+            "calls": calls}
+
+
+def run_read_copies(torch, R, dev, steps=10):
+    """The headline window with a bf16 and with an E4M3 read copy of the checkpoint."""
+    w = WORKLOAD
+    L = w["L"]
+    A, D = sg.head_params(w["nheads"], 0)
+    y = torch.empty(w["batch"], w["nheads"], w["headdim"], device="cuda")
+    out = {}
+    for name, rc, rcb in (("bf16", R.REPLAY_RC_BF16, 2), ("e4m3", R.REPLAY_RC_FP8E4M3, 1)):
+        cfg = R.ReplayConfig(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], L, 0,
+                             R.REPLAY_BF16, rc)
+        st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
+        for _ in range(2):
+            for t in range(L):
+                st.step(*dev[t], y)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps * L)]
+        torch.cuda.synchronize()
+        for k in range(steps):
+            for t in range(L):
+                ev[k * L + t][0].record()
+                st.step(*dev[t], y)
+                ev[k * L + t][1].record()
+        torch.cuda.synchronize()
+        us = np.array([a.elapsed_time(b) for a, b in ev]).reshape(steps, L) * 1e3
+        nf_bytes = sum(step_bytes(w, t, False, rc_bytes=rcb) for t in range(L - 1))
+        fl_bytes = step_bytes(w, L - 1, True, rc_bytes=rcb)
+        out[name] = {"tokens_per_s": w["batch"] * L / (us.sum(axis=1).mean() * 1e-6),
+                     "nonflush_launch_us": float(us[:, :-1].mean()),
+                     "flush_launch_us": float(us[:, -1].mean()),
+                     "nonflush_achieved_gbs": nf_bytes / (us[:, :-1].sum(axis=1).mean() * 1e-6) / 1e9,
+                     "flush_achieved_gbs": fl_bytes / (us[:, -1].mean() * 1e-6) / 1e9}
+        assert st.status() == 0
+        st.close()
+        del st
+    return out
 
 
 # ------------------------------------------------------------------ the oracle (CPU)
@@ -381,6 +495,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="replayssm", choices=["replayssm", "reference"])
     ap.add_argument("--cpu-sample-seqs", type=int, default=8)
     ap.add_argument("--cpu-sample-tokens", type=int, default=48)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the secondary workloads (read copies, speculative verify)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
     rank, world, local_rank = dist_env()

@@ -6,14 +6,7 @@
 #include <new>
 
 #include "launch.h"
-
-struct replay_store {
-  replay_config cfg;
-  replay_layout lay;
-  char* ws;
-  rssm::StoreView sv;
-  rssm::Shape sh;
-};
+#include "store.h"
 
 namespace {
 
@@ -31,12 +24,16 @@ int check_shape(const replay_config* c) {
   if (c->in_dtype != REPLAY_F32 && c->in_dtype != REPLAY_BF16) return REPLAY_EBADARG;
   if (!shape_supported(c->headdim, c->dstate)) return REPLAY_EUNSUPPORTED;
   if (static_cast<long long>(c->batch) * c->nheads > INT_MAX) return REPLAY_ECAPACITY;
+  if (c->batch > 65535 || c->nheads / c->ngroups > 65535) return REPLAY_ECAPACITY;  // grid limits
   return REPLAY_OK;
 }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 int cuda_ok(cudaError_t e) { return e == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA; }
+
+// x, B, C and states are read with 16-byte vector loads and asynchronous copies.
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
 }  // namespace
 
@@ -168,6 +165,7 @@ int replay_step(replay_store* st, const void* x, const void* B, const void* C, c
                 float* y, void* stream) {
   if (st == nullptr || x == nullptr || B == nullptr || C == nullptr || dt == nullptr || y == nullptr)
     return REPLAY_EBADARG;
+  if (!aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
   return rssm::launch_step(st->sv, st->sh, x, B, C, dt, y, as_stream(stream));
 }
 
@@ -175,7 +173,7 @@ int replay_verify(replay_store* st, int T, const void* x, const void* B, const v
                   const void* dt, float* y, void* stream) {
   if (st == nullptr || x == nullptr || B == nullptr || C == nullptr || dt == nullptr || y == nullptr)
     return REPLAY_EBADARG;
-  if (T < 1) return REPLAY_EBADARG;
+  if (T < 1 || !aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
   if (T > st->cfg.max_draft_T) return REPLAY_ECAPACITY;
   return rssm::launch_verify(st->sv, st->sh, T, x, B, C, dt, y, as_stream(stream));
 }
@@ -209,6 +207,7 @@ int conv_step(const replay_config* c, void* state, int state_dtype, const float*
       dt == nullptr || y == nullptr)
     return REPLAY_EBADARG;
   if (state_dtype != REPLAY_F32 && state_dtype != REPLAY_BF16) return REPLAY_EBADARG;
+  if (!aligned16(state) || !aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
   const rssm::Shape sh{c->headdim, c->dstate, c->in_dtype, REPLAY_RC_NONE};
   return rssm::launch_conv_step(sh, c->batch, c->nheads, c->ngroups, state, state_dtype, A, D, x, B, C,
                                 dt, y, as_stream(stream));
@@ -222,6 +221,7 @@ int conv_verify_snapshot(const replay_config* c, int T, float* snaps, const int*
   if (snaps == nullptr || cur == nullptr || A == nullptr || D == nullptr || x == nullptr || B == nullptr ||
       C == nullptr || dt == nullptr || y == nullptr || T < 1)
     return REPLAY_EBADARG;
+  if (!aligned16(snaps) || !aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
   const rssm::Shape sh{c->headdim, c->dstate, c->in_dtype, REPLAY_RC_NONE};
   return rssm::launch_conv_verify(sh, c->batch, c->nheads, c->ngroups, T, snaps, cur, A, D, x, B, C, dt,
                                   y, as_stream(stream));

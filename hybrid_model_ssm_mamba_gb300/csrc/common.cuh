@@ -321,11 +321,20 @@ __device__ __forceinline__ int ring_slot(int start, int s, int cap) {
 
 __device__ __forceinline__ void set_status(int* status, int bit) { atomicOr(status, bit); }
 
+// 16-byte asynchronous global -> shared copy (L2 only), and the wait for all of a thread's
+// outstanding copies. Both addresses must be 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 // Last-CTA-done update of a sequence's metadata: every CTA of sequence b calls this once,
-// after its single reader thread has read meta[b]; the last of the H arrivals writes the
-// new value and re-arms the counter. Nothing waits, so nothing can hang.
+// from its single reader thread, after the value it read from meta[b] has been consumed
+// (written to shared memory and past a CTA barrier), so its read is complete; the last of
+// the H arrivals writes the new value and re-arms the counter. The new value is only read
+// by later launches. Nothing waits, so nothing can hang.
 __device__ __forceinline__ void arrive_and_publish(const StoreView& sv, int b, int4 next) {
-  __threadfence();
   const int old = atomicAdd(&sv.arrive[b], 1);
   if (old == sv.H - 1) {
     sv.arrive[b] = 0;

@@ -1,12 +1,13 @@
-// Device routines shared by the step, verify and flush kernels: folding buffered records
-// into a checkpoint tile, and writing a new checkpoint with its read copy.
+// Device routines shared by the step, verify and flush kernels: staging a slab's records
+// in shared memory, folding them into a checkpoint tile, writing a new checkpoint with its
+// read copy, and the per-warp record weights.
 #pragma once
 
 #include "common.cuh"
 
 namespace rssm {
 
-// Pointers to one (sequence, head) slab's ring records.
+// Pointers to one (sequence, head) slab's ring records in global memory.
 template <class T>
 struct SlabRing {
   T* x;   // [cap][P] of this head
@@ -24,75 +25,131 @@ __device__ __forceinline__ SlabRing<T> slab_ring(const StoreView& sv, int b, int
   return r;
 }
 
-// Fold K records into the register tile of the checkpoint ("How ReplaySSM represents the
-// state": the state after a window is the cumulative decay times the state before it plus
-// the buffered records):
-//     h <- Gamma_K * h + sum_{s<K} w_s x_s B_s^T,  w_s = exp(A sum_{r=s+1..K-1} dt_r) dt_s,
-//     Gamma_K = exp(A sum_{r<K} dt_r).
-// Records s < nring are ring slots (start + s) mod cap; record s == nring, when K > nring,
-// is the current token (xcur, bcur, dtcur). The records are staged in shared memory as FP32
-// (sm_x [K][P], sm_b [K][N], sm_dt [K]); every thread then forms its own w_s, so the suffix
-// sums of dt are taken directly over each range, as in the definition. Starts and ends with
-// a CTA barrier.
+// Shared-memory image of a slab's records. In a ring image the slots are those of the global
+// ring, so record s of the window sits at slot (start + s) mod cap in both.
+template <class T>
+struct RingImage {
+  T* x;       // [slots][P]
+  T* b;       // [slots][N]
+  float* dt;  // [slots]
+};
+
 template <int P, int N, class T>
-__device__ __forceinline__ void fold_records(const SlabRing<T>& ring, int start, int cap, int K,
-                                             int nring, const T* xcur, const T* bcur, T dtcur,
-                                             float A, float* sm_x, float* sm_b, float* sm_dt,
-                                             float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
-  using TL = Tile<P, N>;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  __syncthreads();  // shared staging buffers may still be read by an earlier phase
-  for (int idx = tid; idx < K * P; idx += kThreads) {
-    const int s = idx / P, p = idx - s * P;
-    sm_x[idx] = s < nring ? to_f(ring.x[static_cast<size_t>(ring_slot(start, s, cap)) * P + p])
-                          : to_f(xcur[p]);
-  }
-  for (int idx = tid; idx < K * N; idx += kThreads) {
-    const int s = idx / N, c = idx - s * N;
-    sm_b[idx] = s < nring ? to_f(ring.b[static_cast<size_t>(ring_slot(start, s, cap)) * N + c])
-                          : to_f(bcur[c]);
-  }
-  if (tid < K) sm_dt[tid] = tid < nring ? to_f(ring.dt[ring_slot(start, tid, cap)]) : to_f(dtcur);
-  __syncthreads();
+__host__ __device__ constexpr size_t ring_image_bytes(int cap) {
+  return static_cast<size_t>(cap) * (P + N) * sizeof(T) + static_cast<size_t>(cap) * sizeof(float);
+}
 
-  float tot = 0.f;
-  for (int r = 0; r < K; ++r) tot += sm_dt[r];
-  const float Gam = expf(A * tot);
-#pragma unroll
-  for (int i = 0; i < TL::RPW; ++i)
-#pragma unroll
-    for (int e = 0; e < TL::E; ++e) hv[i][e] *= Gam;
+template <int P, int N, class T>
+__device__ __forceinline__ RingImage<T> ring_image(void* smem, int cap) {
+  RingImage<T> im;
+  im.x = static_cast<T*>(smem);
+  im.b = im.x + static_cast<size_t>(cap) * P;
+  im.dt = reinterpret_cast<float*>(im.b + static_cast<size_t>(cap) * N);
+  return im;
+}
 
-  float suf = 0.f;  // sum of dt over records after s
-  for (int s = K - 1; s >= 0; --s) {
-    const float dts = sm_dt[s];
-    const float w = expf(A * suf) * dts;
-    suf += dts;
-    float u[TL::RPW];
-#pragma unroll
-    for (int i = 0; i < TL::RPW; i += 4) {
-      const float4 t = *reinterpret_cast<const float4*>(sm_x + s * P + warp * TL::RPW + i);
-      u[i] = w * t.x; u[i + 1] = w * t.y; u[i + 2] = w * t.z; u[i + 3] = w * t.w;
+// Where the records of a window come from: s < nring are ring slots; s >= nring are "extra"
+// records held by the caller's input arrays (the drafts of a verify), extra record e at
+// x + e*xstride, b + e*bstride, dt[e*dtstride].
+template <class T>
+struct ExtraRecords {
+  const T* x;
+  const T* b;
+  const T* dt;
+  size_t xstride, bstride, dtstride;
+};
+
+// Copy records s = 0..K-1 of the window into the ring image with 16-byte cp.async chunks
+// (all threads), and their dt values as FP32. The caller waits with cp_async_wait_all() and
+// a CTA barrier before reading the image.
+template <int P, int N, class T>
+__device__ __forceinline__ void stage_records(const SlabRing<T>& ring, const RingImage<T>& im,
+                                              int start, int cap, int K, int nring,
+                                              const ExtraRecords<T>& ex) {
+  constexpr int EPC = 16 / sizeof(T);  // elements per 16-byte chunk
+  constexpr int XC = P / EPC, BC = N / EPC;
+  static_assert(P % EPC == 0 && N % EPC == 0, "records must be whole 16-byte chunks");
+  const int nx = K * XC, total = K * (XC + BC);
+  for (int c = threadIdx.x; c < total; c += kThreads) {
+    if (c < nx) {
+      const int s = c / XC, off = (c - s * XC) * EPC;
+      const int slot = ring_slot(start, s, cap);
+      const T* src = s < nring ? ring.x + static_cast<size_t>(slot) * P : ex.x + (s - nring) * ex.xstride;
+      cp_async16(im.x + slot * P + off, src + off);
+    } else {
+      const int c2 = c - nx;
+      const int s = c2 / BC, off = (c2 - s * BC) * EPC;
+      const int slot = ring_slot(start, s, cap);
+      const T* src = s < nring ? ring.b + static_cast<size_t>(slot) * N : ex.b + (s - nring) * ex.bstride;
+      cp_async16(im.b + slot * N + off, src + off);
     }
-    float bv[TL::E];
-#pragma unroll
-    for (int v = 0; v < TL::NVEC; ++v) {
-      float t[TL::VEC];
-      ldv<TL::VEC>(sm_b + s * N + TL::col(lane, v), t);
-#pragma unroll
-      for (int e = 0; e < TL::VEC; ++e) bv[v * TL::VEC + e] = t[e];
-    }
-#pragma unroll
-    for (int i = 0; i < TL::RPW; ++i)
-#pragma unroll
-      for (int e = 0; e < TL::E; ++e) hv[i][e] = fmaf(u[i], bv[e], hv[i][e]);
   }
-  __syncthreads();
+  for (int s = threadIdx.x; s < K; s += kThreads)
+    im.dt[ring_slot(start, s, cap)] =
+        to_f(s < nring ? ring.dt[ring_slot(start, s, cap)] : ex.dt[(s - nring) * ex.dtstride]);
+}
+
+// Whole-ring image for the decode step: image slots 0..cap-1 hold a copy of the slab's ring
+// (x per head, B per group, dt) and slot cap holds the current token's record, so staging
+// needs no ring pointer and starts together with the checkpoint loads. Record s of the
+// window sits at image slot (start + s) mod cap for s < n and at slot cap for s == n.
+template <int P, int N, class T>
+__host__ __device__ constexpr size_t whole_image_bytes(int cap) {
+  return static_cast<size_t>(cap + 1) * (P + N) * sizeof(T) + static_cast<size_t>(cap + 1) * sizeof(float);
+}
+
+template <int P, int N, class T>
+__device__ __forceinline__ RingImage<T> whole_image(void* smem, int cap) {
+  RingImage<T> im;
+  im.x = static_cast<T*>(smem);
+  im.b = im.x + static_cast<size_t>(cap + 1) * P;
+  im.dt = reinterpret_cast<float*>(im.b + static_cast<size_t>(cap + 1) * N);
+  return im;
+}
+
+template <int P, int N, class T>
+__device__ __forceinline__ void stage_whole_ring(const SlabRing<T>& ring, const RingImage<T>& im, int cap,
+                                                 const T* xcur, const T* bcur, T dtcur) {
+  constexpr int EPC = 16 / sizeof(T);
+  constexpr int XC = P / EPC, BC = N / EPC;  // 16-byte chunks per record
+  const int nx = (cap + 1) * XC, total = nx + (cap + 1) * BC;
+  for (int c = threadIdx.x; c < total; c += kThreads) {
+    if (c < nx) {
+      const int s = c / XC, off = (c - s * XC) * EPC;
+      cp_async16(im.x + s * P + off, (s < cap ? ring.x + static_cast<size_t>(s) * P : xcur) + off);
+    } else {
+      const int c2 = c - nx;
+      const int s = c2 / BC, off = (c2 - s * BC) * EPC;
+      cp_async16(im.b + s * N + off, (s < cap ? ring.b + static_cast<size_t>(s) * N : bcur) + off);
+    }
+  }
+  for (int s = threadIdx.x; s <= cap; s += kThreads) im.dt[s] = to_f(s < cap ? ring.dt[s] : dtcur);
+}
+
+// Copy one record (x of this head, B of this group if `with_b`) from image slot `from` to
+// global ring slot `to` with 16-byte vectors, and dt from `dtv`.
+template <int P, int N, class T>
+__device__ __forceinline__ void append_record(const SlabRing<T>& ring, const RingImage<T>& im, int from,
+                                              int to, bool with_b, T dtv) {
+  constexpr int EPC = 16 / sizeof(T);
+  constexpr int XC = P / EPC, BC = N / EPC;
+  const int t = threadIdx.x;
+  if (t < XC) {
+    *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(to) * P + t * EPC) =
+        *reinterpret_cast<const uint4*>(im.x + from * P + t * EPC);
+  } else if (with_b && t < XC + BC) {
+    const int c = t - XC;
+    *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(to) * N + c * EPC) =
+        *reinterpret_cast<const uint4*>(im.b + from * N + c * EPC);
+  } else if (t == XC + BC) {
+    ring.dt[to] = dtv;
+  }
 }
 
 // Write a new checkpoint tile: FP32 always, and the read copy cast independently from the
 // same FP32 values ("Benefit 3: Limit error accumulation with separate precisions"). The
-// E4M3 copy takes one FP32 scale per slab, absmax / 448 (1 for an all-zero slab).
+// E4M3 copy takes one FP32 scale per slab, absmax / 448 (1 for an all-zero slab). Contains
+// CTA barriers when the copy is E4M3.
 template <int P, int N, int RC>
 __device__ __forceinline__ void write_checkpoint(const StoreView& sv, size_t slab, float* s_red,
                                                  const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
@@ -120,8 +177,8 @@ __device__ __forceinline__ void write_checkpoint(const StoreView& sv, size_t sla
   }
 }
 
-// Output of the tile's rows against the lane's columns of c: y[row] = gam * (h . c)[row]
-// + extra[row], reduced across the warp; the transpose leader of each row gets the value.
+// Output of the tile's rows against the lane's columns of c: gam * (h . c)[row] + extra[row],
+// reduced across the warp; the transpose leader of each row gets the value.
 template <int P, int N>
 __device__ __forceinline__ float tile_rows_dot(const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E],
                                                const float (&cv)[Tile<P, N>::E], float gam,
@@ -136,6 +193,106 @@ __device__ __forceinline__ float tile_rows_dot(const float (&hv)[Tile<P, N>::RPW
     part[i] = fmaf(gam, hc, extra[i]);
   }
   return warp_transpose_reduce<TL::RPW>(part, lane);
+}
+
+// Weights of the records of one query, one record per lane (record s = lane, and lane+32
+// when k > 32): w_s = exp(A sum_{r=s+1..k-1} dt_r) * dt_s, Gamma = exp(A sum_{r<k} dt_r).
+// The suffix sums are warp scans (tree order) over the records' dt, each over its own range.
+// exp is the fast hardware exponential (__expf): its relative error, a few 1e-7 at the
+// exponents met here, is far inside the 1e-4 output bound.
+struct RecordWeights {
+  float w0, w1, gam;
+};
+__device__ __forceinline__ float suffix_scan(float v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float a = __shfl_down_sync(kFull, v, off);
+    if (lane + off < 32) v += a;
+  }
+  return v;  // inclusive: sum over lanes >= lane
+}
+__device__ __forceinline__ RecordWeights record_weights(float dt0, float dt1, int k, float A, int lane) {
+  // dt0: record lane (0 if lane >= k); dt1: record lane + 32 (0 if lane + 32 >= k)
+  RecordWeights r;
+  const float in0 = suffix_scan(dt0, lane);
+  float ex0 = __shfl_down_sync(kFull, in0, 1);  // exclusive: the records after s
+  if (lane == 31) ex0 = 0.f;
+  float tot1 = 0.f;
+  r.w1 = 0.f;
+  if (k > 32) {  // warp-uniform
+    const float in1 = suffix_scan(dt1, lane);
+    float ex1 = __shfl_down_sync(kFull, in1, 1);
+    if (lane == 31) ex1 = 0.f;
+    tot1 = __shfl_sync(kFull, in1, 0);
+    ex0 += tot1;  // records 32..k-1 follow every record of the lower half
+    r.w1 = lane + 32 < k ? __expf(A * ex1) * dt1 : 0.f;
+  }
+  r.w0 = lane < k ? __expf(A * ex0) * dt0 : 0.f;
+  r.gam = __expf(A * (__shfl_sync(kFull, in0, 0) + tot1));
+  return r;
+}
+
+// Fold K records into the register tile of the checkpoint, record s at image slot
+// slot_of(s) ("How ReplaySSM represents the state": the state after a window is the
+// cumulative decay times the state before it, plus the buffered records):
+//     h <- Gamma_K * h + sum_{s<K} w_s x_s B_s^T,  w_s = exp(A sum_{r=s+1..K-1} dt_r) dt_s.
+// Warp 0 forms the weights by warp scans; the CTA then stages u_s = w_s x_s and B_s in FP32
+// (sm_u [K][P], sm_b [K][N]) so the rank-K update is three 16-byte shared loads and 32 FFMA
+// per record per thread. Contains CTA barriers; s_w holds kMaxCap + 1 floats.
+template <int P, int N, class T, class SlotOf>
+__device__ __forceinline__ void fold_tile(const RingImage<T>& im, SlotOf slot_of, int K, float A,
+                                          float* sm_u, float* sm_b, float* s_w,
+                                          float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    const float dt0 = lane < K ? im.dt[slot_of(lane)] : 0.f;
+    const float dt1 = lane + 32 < K ? im.dt[slot_of(lane + 32)] : 0.f;
+    const RecordWeights rw = record_weights(dt0, dt1, K, A, lane);
+    if (lane < K) s_w[lane] = rw.w0;
+    if (lane + 32 < K) s_w[lane + 32] = rw.w1;
+    if (lane == 0) s_w[kMaxCap] = rw.gam;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < K * P; idx += kThreads) {
+    const int s = idx / P, p = idx - s * P;
+    sm_u[idx] = s_w[s] * to_f(im.x[slot_of(s) * P + p]);
+  }
+  for (int idx = tid; idx < K * N; idx += kThreads) {
+    const int s = idx / N, c = idx - s * N;
+    sm_b[idx] = to_f(im.b[slot_of(s) * N + c]);
+  }
+  __syncthreads();
+  const float Gam = s_w[kMaxCap];
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+    for (int e = 0; e < TL::E; ++e) hv[i][e] *= Gam;
+  for (int s = 0; s < K; ++s) {
+    float u[TL::RPW], bv[TL::E];
+    load_rows<TL::RPW>(sm_u + s * P + warp * TL::RPW, u);
+    load_cols<P, N>(sm_b + s * N, lane, bv);
+#pragma unroll
+    for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+      for (int e = 0; e < TL::E; ++e) hv[i][e] = fmaf(u[i], bv[e], hv[i][e]);
+  }
+}
+
+template <int P, int N>
+__host__ __device__ constexpr size_t fold_staging_bytes(int K) {
+  return static_cast<size_t>(K) * (P + N) * sizeof(float);
+}
+
+// Shared-memory plan of a kernel: a record image of `image_bytes`, then (128-byte aligned)
+// the FP32 staging of a fold of up to `cap` records.
+__host__ __device__ constexpr size_t align128(size_t v) { return (v + 127) / 128 * 128; }
+template <int P, int N>
+__host__ __device__ constexpr size_t smem_plan_bytes(size_t image_bytes, int cap) {
+  return align128(image_bytes) + fold_staging_bytes<P, N>(cap);
+}
+__device__ __forceinline__ float* fold_staging(void* smem, size_t image_bytes) {
+  return reinterpret_cast<float*>(static_cast<char*>(smem) + align128(image_bytes));
 }
 
 }  // namespace rssm

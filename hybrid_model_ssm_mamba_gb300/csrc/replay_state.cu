@@ -17,13 +17,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<N>)
 replay_fold_kernel(StoreView sv, float* __restrict__ out) {
   using TL = Tile<P, N>;
   extern __shared__ float4 smem4[];
-  float* smem = reinterpret_cast<float*>(smem4);
   __shared__ int4 s_meta;
-  __shared__ float s_dt[kMaxCap];
+  __shared__ float s_w[kMaxCap + 1];
   __shared__ float s_red[kWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slab = blockIdx.x;
-  const int b = slab / sv.H, h = slab - b * sv.H, g = h / sv.hpg;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int h = g * sv.hpg + blockIdx.x;
+  const int slab = b * sv.H + h;
   const int cap = sv.cap;
 
   if (tid == 0) s_meta = sv.meta[b];
@@ -42,16 +42,24 @@ replay_fold_kernel(StoreView sv, float* __restrict__ out) {
     }
     return;
   }
+  const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+  const RingImage<T> im = ring_image<P, N, T>(smem4, cap);
+  const ExtraRecords<T> none{nullptr, nullptr, nullptr, 0, 0, 0};
+  stage_records<P, N, T>(ring, im, start, cap, n, n, none);
+  if constexpr (MODE == 0) {
+    if (tid == 0) arrive_and_publish(sv, b, make_int4(ring_slot(start, n, cap), 0, 0, 0));
+  }
+  cp_async_wait_all();
+  __syncthreads();
   if (n > 0) {
-    const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
-    fold_records<P, N, T>(ring, start, cap, n, n, nullptr, nullptr, T(0.f), sv.A[h], smem,
-                          smem + cap * P, s_dt, hv);
+    auto slot_of = [&](int s) { return ring_slot(start, s, cap); };
+    float* sm_u = fold_staging(smem4, ring_image_bytes<P, N, T>(cap));
+    fold_tile<P, N, T>(im, slot_of, n, sv.A[h], sm_u, sm_u + cap * P, s_w, hv);
   }
   if constexpr (MODE == 1) {
     store_tile_f32<P, N>(out + static_cast<size_t>(slab) * P * N, warp, lane, hv);
   } else {
     if (n > 0) write_checkpoint<P, N, RC>(sv, slab, s_red, hv);
-    if (tid == 0) arrive_and_publish(sv, b, make_int4(ring_slot(start, n, cap), 0, 0, 0));
   }
 }
 
@@ -83,13 +91,14 @@ replay_load_kernel(StoreView sv, const float* __restrict__ h, const int* __restr
 
 template <int P, int N, class T, int RC>
 static int fold(const StoreView& sv, int mode, float* out, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(sv.cap) * (P + N) * sizeof(float);
+  const size_t smem = smem_plan_bytes<P, N>(ring_image_bytes<P, N, T>(sv.cap), sv.cap);
   auto kern = mode == 0 ? replay_fold_kernel<P, N, T, RC, 0> : replay_fold_kernel<P, N, T, RC, 1>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
-  kern<<<sv.batch * sv.H, kThreads, smem, stream>>>(sv, out);
+  const dim3 grid(sv.hpg, sv.G, sv.batch);
+  kern<<<grid, kThreads, smem, stream>>>(sv, out);
   return cudaGetLastError() == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA;
 }
 

@@ -8,6 +8,12 @@
 // overwritten, and a flush folds only committed records. The T outputs are computed by
 // output-only evaluation: the checkpoint is read once for all T queries and every other
 // term is a scalar (B_s . C_j, times a decay) scaling a cached x_s -- no state is formed.
+//
+// One CTA per (sequence, head) slab, as in the step kernel: the checkpoint tile is loaded
+// into registers first; the committed records and the drafts are staged in a shared-memory
+// image of the ring (the drafts at the slots they are appended to); when n >= L committed
+// records are waiting they are folded into the tile and written as the new checkpoint
+// before the drafts are evaluated.
 #include "launch.h"
 #include "replay_core.cuh"
 
@@ -22,16 +28,16 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
   using TL = Tile<P, N>;
   constexpr int RPW = TL::RPW, E = TL::E;
   extern __shared__ float4 smem4[];
-  float* smem = reinterpret_cast<float*>(smem4);
   __shared__ int4 s_meta;
-  __shared__ float s_dt[kMaxCap];
   __shared__ float s_bc[kMaxDrafts][kMaxCap];
+  __shared__ float s_w[kMaxCap + 1];
   __shared__ float s_red[kWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slab = blockIdx.x;
   const int H = sv.H, G = sv.G;
-  const int b = slab / H, h = slab - b * H, g = h / sv.hpg;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int h = g * sv.hpg + blockIdx.x;
+  const int slab = b * H + h;
   const int cap = sv.cap;
   // draft j of sequence b: x/y at ((b*TT + j)*H + h)*P, B/C at ((b*TT + j)*G + g)*N
   auto xoff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * H * P + static_cast<size_t>(h) * P; };
@@ -40,8 +46,14 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
 
   if (tid == 0) s_meta = sv.meta[b];
   float hv[RPW][E];
-  if constexpr (RC == REPLAY_RC_NONE)
+  if constexpr (RC == REPLAY_RC_NONE) {
     load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+  } else {
+    const float scale = RC == REPLAY_RC_FP8E4M3 ? sv.scale[slab] : 1.f;
+    load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv);
+  }
+  const int myrow = warp * RPW + transpose_index<RPW>(lane);
+  const float A = sv.A[h], Dh = sv.D[h];
   __syncthreads();
 
   const int start = s_meta.x, n = s_meta.y;
@@ -51,37 +63,34 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
     if (tid == 0) set_status(sv.status, REPLAY_DEV_BAD_META);
     return;
   }
-  const float A = sv.A[h], Dh = sv.D[h];
+  const bool prefold = n >= sv.L;  // fold the committed records first (flush of committed only)
+  const int start2 = prefold ? ring_slot(start, n, cap) : start;
+  const int n2 = prefold ? 0 : n;
   const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
-  int start2 = start, n2 = n;
-  if (n >= sv.L) {
-    // fold the committed records first (a flush of committed records only)
-    if constexpr (RC != REPLAY_RC_NONE)
-      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
-    fold_records<P, N, T>(ring, start, cap, n, n, nullptr, nullptr, T(0.f), A, smem, smem + cap * P,
-                          s_dt, hv);
-    write_checkpoint<P, N, RC>(sv, slab, s_red, hv);
-    start2 = ring_slot(start, n, cap);
-    n2 = 0;
-    __syncthreads();  // s_dt is reused below
-  } else {
-    if constexpr (RC != REPLAY_RC_NONE) {
-      const float scale = RC == REPLAY_RC_FP8E4M3 ? sv.scale[slab] : 1.f;
-      load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv);
-    }
+  const RingImage<T> im = ring_image<P, N, T>(smem4, cap);
+  const ExtraRecords<T> drafts{x + xoff(0), B + boff(0), dt + doff(0), static_cast<size_t>(H) * P,
+                               static_cast<size_t>(G) * N, static_cast<size_t>(H)};
+  stage_records<P, N, T>(ring, im, start, cap, n + TT, n, drafts);
+  if (tid == 0) arrive_and_publish(sv, b, make_int4(start2, n2, TT, 0));
+  if constexpr (RC != REPLAY_RC_NONE) {
+    if (prefold) load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
   }
+  cp_async_wait_all();
+  __syncthreads();
 
-  const int kk = n2 + TT;  // committed records, then the drafts
-  if (warp == kWarps - 1)
-    for (int s = lane; s < kk; s += 32)
-      s_dt[s] = s < n2 ? to_f(ring.dt[ring_slot(start2, s, cap)]) : to_f(dt[doff(s - n2)]);
+  if (prefold) {
+    auto slot_of = [&](int s) { return ring_slot(start, s, cap); };
+    float* sm_u = fold_staging(smem4, ring_image_bytes<P, N, T>(cap));
+    fold_tile<P, N, T>(im, slot_of, n, A, sm_u, sm_u + cap * P, s_w, hv);
+    write_checkpoint<P, N, RC>(sv, slab, s_red, hv);
+  }
+  const int kk = n2 + TT;  // committed records, then the drafts, from slot start2
   // B_s . C_j for every record s a draft j sees (s <= n2 + j); the pair loop is warp-strided
   for (int pi = warp; pi < TT * kk; pi += kWarps) {
     const int j = pi / kk, s = pi - j * kk;
     if (s > n2 + j) continue;
-    const T* bs = s < n2 ? ring.b + static_cast<size_t>(ring_slot(start2, s, cap)) * N : B + boff(s - n2);
     float bv[E], cj[E];
-    load_cols<P, N>(bs, lane, bv);
+    load_cols<P, N>(im.b + ring_slot(start2, s, cap) * N, lane, bv);
     load_cols<P, N>(C + boff(j), lane, cj);
     float d = 0.f;
 #pragma unroll
@@ -89,75 +98,50 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
     d = warp_sum(d);
     if (lane == 0) s_bc[j][s] = d;
   }
-  float xr[RPW];  // record `lane`: x values of this warp's rows
-  const int s0 = lane;
-  if (s0 < kk) {
-    const T* xs = s0 < n2 ? ring.x + static_cast<size_t>(ring_slot(start2, s0, cap)) * P : x + xoff(s0 - n2);
-    load_rows<RPW>(xs + warp * RPW, xr);
-  } else {
-#pragma unroll
-    for (int i = 0; i < RPW; ++i) xr[i] = 0.f;
-  }
   __syncthreads();
 
+  float xr0[RPW], xr1[RPW];  // records lane and lane + 32: x values of this warp's rows
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) xr0[i] = xr1[i] = 0.f;
+  if (lane < kk) load_rows<RPW>(im.x + ring_slot(start2, lane, cap) * P + warp * RPW, xr0);
+  if (lane + 32 < kk) load_rows<RPW>(im.x + ring_slot(start2, lane + 32, cap) * P + warp * RPW, xr1);
+  const float dt0 = lane < kk ? im.dt[ring_slot(start2, lane, cap)] : 0.f;
+  const float dt1 = lane + 32 < kk ? im.dt[ring_slot(start2, lane + 32, cap)] : 0.f;
   for (int j = 0; j < TT; ++j) {
     const int k = n2 + j + 1;  // records draft j sees, itself included
-    float tot = 0.f;
-    for (int r = 0; r < k; ++r) tot += s_dt[r];
-    const float Gam = expf(A * tot);
-    float c0 = 0.f;
-    if (s0 < k) {
-      float suf = 0.f;
-      for (int r = s0 + 1; r < k; ++r) suf += s_dt[r];
-      c0 = expf(A * suf) * s_dt[s0] * s_bc[j][s0];
-    }
+    const RecordWeights rw = record_weights(lane < k ? dt0 : 0.f, lane + 32 < k ? dt1 : 0.f, k, A, lane);
+    const float c0 = lane < k ? rw.w0 * s_bc[j][lane] : 0.f;
+    const float c1 = lane + 32 < k ? rw.w1 * s_bc[j][lane + 32] : 0.f;
     float ex[RPW];
 #pragma unroll
-    for (int i = 0; i < RPW; ++i) ex[i] = c0 * xr[i];
-    if (k > 32) {
-      const int s1 = lane + 32;
-      if (s1 < k) {
-        const T* xs = s1 < n2 ? ring.x + static_cast<size_t>(ring_slot(start2, s1, cap)) * P : x + xoff(s1 - n2);
-        float x1[RPW];
-        load_rows<RPW>(xs + warp * RPW, x1);
-        float suf = 0.f;
-        for (int r = s1 + 1; r < k; ++r) suf += s_dt[r];
-        const float c1 = expf(A * suf) * s_dt[s1] * s_bc[j][s1];
-#pragma unroll
-        for (int i = 0; i < RPW; ++i) ex[i] = fmaf(c1, x1[i], ex[i]);
-      }
-    }
+    for (int i = 0; i < RPW; ++i) ex[i] = fmaf(c1, xr1[i], c0 * xr0[i]);
     float cq[E];
     load_cols<P, N>(C + boff(j), lane, cq);
-    const float sum = tile_rows_dot<P, N>(hv, cq, Gam, ex, lane);
+    const float sum = tile_rows_dot<P, N>(hv, cq, rw.gam, ex, lane);
     if (transpose_leader<RPW>(lane)) {
-      const int row = warp * RPW + transpose_index<RPW>(lane);
-      y[xoff(j) + row] = fmaf(Dh, to_f(x[xoff(j) + row]), sum);
+      const float xj = to_f(im.x[ring_slot(start2, n2 + j, cap) * P + myrow]);
+      y[xoff(j) + myrow] = fmaf(Dh, xj, sum);
     }
   }
-  // the drafts' records go beyond the committed ones; the pointer stays
+  // the drafts' records go to the ring beyond the committed ones; the pointer stays
   for (int j = 0; j < TT; ++j) {
     const int slot = ring_slot(start2, n2 + j, cap);
-    for (int p = tid; p < P; p += kThreads) ring.x[static_cast<size_t>(slot) * P + p] = x[xoff(j) + p];
-    if (h % sv.hpg == 0)
-      for (int c = tid; c < N; c += kThreads) ring.b[static_cast<size_t>(slot) * N + c] = B[boff(j) + c];
-    if (tid == 0) ring.dt[slot] = dt[doff(j)];
+    append_record<P, N, T>(ring, im, slot, slot, blockIdx.x == 0, dt[doff(j)]);
   }
-  if (tid == 0) arrive_and_publish(sv, b, make_int4(start2, n2, TT, 0));
 }
 
 template <int P, int N, class T, int RC>
 static int launch(const StoreView& sv, int TT, const void* x, const void* B, const void* C,
                   const void* dt, float* y, cudaStream_t stream) {
   auto kern = replay_verify_kernel<P, N, T, RC>;
-  const size_t smem = static_cast<size_t>(sv.cap) * (P + N) * sizeof(float);
+  const size_t smem = smem_plan_bytes<P, N>(ring_image_bytes<P, N, T>(sv.cap), sv.cap);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
-  kern<<<sv.batch * sv.H, kThreads, smem, stream>>>(sv, TT, static_cast<const T*>(x),
-                                                   static_cast<const T*>(B), static_cast<const T*>(C),
-                                                   static_cast<const T*>(dt), y);
+  const dim3 grid(sv.hpg, sv.G, sv.batch);
+  kern<<<grid, kThreads, smem, stream>>>(sv, TT, static_cast<const T*>(x), static_cast<const T*>(B),
+                                         static_cast<const T*>(C), static_cast<const T*>(dt), y);
   return cudaGetLastError() == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA;
 }
 

@@ -32,6 +32,8 @@
  *      y [batch][T][H][P]                                                     (T drafts)
  *      A, D [H] FP32 on the device; states [batch][H][P][N] FP32.
  *    x, B, C and dt are FP32 or bf16 (replay_config.in_dtype); y is always FP32.
+ *    x, B, C and state buffers must be 16-byte aligned (REPLAY_EBADARG otherwise).
+ *  - Limits: batch <= 65535 (REPLAY_ECAPACITY otherwise).
  *  - Supported shapes: headdim P = 64 and dstate N in {64, 128, 256}; H a multiple of G;
  *    ring capacity (see replay_layout) at most 64 records.
  */
