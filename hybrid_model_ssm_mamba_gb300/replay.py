@@ -32,6 +32,7 @@ HEADER = pathlib.Path(__file__).resolve().parent.parent / "include" / "replayssm
 REPLAY_F32, REPLAY_BF16 = 0, 1
 REPLAY_RC_NONE, REPLAY_RC_BF16, REPLAY_RC_FP8E4M3 = 0, 1, 2
 REPLAY_DEV_BAD_META, REPLAY_DEV_BAD_ACCEPT = 1, 2
+REPLAY_STATIC_MAX_BATCH = 4096
 _ERRORS = {-1: "bad argument", -2: "unsupported shape or dtype", -3: "capacity exceeded",
            -4: "CUDA error"}
 
@@ -73,6 +74,7 @@ _SIGS = {
     "replay_load_state": [_P, _P, _P],
     "replay_export_state": [_P, _P, _P],
     "replay_step": [_P, _P, _P, _P, _P, _P, _P],
+    "replay_step_static_scratch": [_P, _P, _P, _P, _P, _P, _P],
     "replay_verify": [_P, _I, _P, _P, _P, _P, _P, _P],
     "replay_commit": [_P, _P, _P],
     "replay_flush": [_P, _P],
@@ -188,6 +190,14 @@ def replay_commit(store, accept, stream=None):
 
 def replay_flush(store, stream=None):
     _check("replay_flush", load_library().replay_flush(store, _stream(stream)))
+
+
+def replay_step_static_scratch(store, x, B, C, dt, y, stream=None):
+    """replay_step whose scratch (per-sequence arrival counters) lives in a fixed array in
+    the library, for callers that must not allocate device memory; batch is limited to
+    REPLAY_STATIC_MAX_BATCH."""
+    _check("replay_step_static_scratch", load_library().replay_step_static_scratch(
+        store, _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(y), _stream(stream)))
 
 
 def replay_status(store, clear=False, stream=None) -> int:

@@ -170,6 +170,29 @@ int replay_flush(replay_store* st, void* stream);
  * afterwards if `clear` is nonzero. */
 int replay_status(replay_store* st, int* status_out, int clear, void* stream);
 
+/* replay_step for callers that must not allocate device memory. The paper has no
+ * counterpart: this is a deployment aid of this library.
+ * Who needs it: callers that cannot call cudaMalloc (or anything that allocates) when they
+ * decode -- an engine plugin handed only its input, output and state buffers, a process
+ * whose device memory is pre-claimed by another framework's pool, code running while a
+ * stream is captured. replay_step's one piece of scratch memory is a per-sequence arrival
+ * counter; this call keeps those counters in a fixed array inside the library (the store's
+ * `arrive` region is not touched) and is otherwise replay_step: same arguments, kernel,
+ * results and errors.
+ * Limits and rules:
+ *  - batch <= REPLAY_STATIC_MAX_BATCH, else REPLAY_ECAPACITY and nothing is launched. The
+ *    array (REPLAY_STATIC_MAX_BATCH int32, 16 KiB) exists on every GPU that loads the
+ *    library, until the process exits.
+ *  - The first call on a device looks up the array's device address (once per device, with
+ *    that device current); make that first call before any stream capture.
+ *  - Each call zeroes the counters it uses (an asynchronous memset on `stream`, no
+ *    allocation) before its launch. All calls share the one array, so calls on the same
+ *    device that can overlap on the GPU (different streams, no ordering between them) race
+ *    and give wrong results: order them, or use replay_step. */
+#define REPLAY_STATIC_MAX_BATCH 4096
+int replay_step_static_scratch(replay_store* st, const void* x, const void* B, const void* C,
+                               const void* dt, float* y, void* stream);
+
 /* ---------------------------------------------------------------------------------
  * Conventional baselines ("Why SSM layers can become a decoding bottleneck"; "Rollback
  * for speculative decoding"). They use the config's shape fields and in_dtype only.
