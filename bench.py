@@ -311,7 +311,7 @@ def run_replay(args, rank, world, local_rank):
                    "parallelism": f"dp{world} (independent batches)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "replay_step_kernel (window average)",
+                     "kernel": "replay_step (prep + main kernel per token, window average)",
                      "algorithmic_bytes_per_launch": alg_bytes / (args.steps * L),
                      "nonflush_achieved": nf_bytes / nf_s / 1e9,
                      "nonflush_frac": nf_bytes / nf_s / 1e9 / peak,
@@ -319,7 +319,7 @@ def run_replay(args, rank, world, local_rank):
                      "flush_launch_us": float(launch_s[:, -1].mean() * 1e6)},
         "e2e": {"value": world * w["batch"] * L * e_steps / e_el, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * L,
+        "gpu_launches": args.steps * L * 2,
         "baselines": {"conv_step_tokens_per_s": conv_tps,
                       "conv_step_achieved_gbs": conv_bytes(w) / conv_s / 1e9,
                       "replay_speedup_vs_conv": (w["batch"] * L * args.steps / elapsed) / conv_tps},

@@ -82,6 +82,8 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   L.meta = take(Bn * 16);
   L.arrive = take(Bn * 4);
   L.status = take(4);
+  L.plan = take(Bn * 16);
+  L.coef = take(Bn * H * (cap + 1) * 4);
   L.total = off;
   *out = L;
   return REPLAY_OK;
@@ -118,6 +120,8 @@ int replay_alloc(const replay_config* c, void* workspace, size_t workspace_bytes
   sv.meta = reinterpret_cast<int4*>(st->ws + L.meta);
   sv.arrive = reinterpret_cast<int*>(st->ws + L.arrive);
   sv.status = reinterpret_cast<int*>(st->ws + L.status);
+  sv.plan = reinterpret_cast<int4*>(st->ws + L.plan);
+  sv.coef = reinterpret_cast<float*>(st->ws + L.coef);
   sv.A = A;
   sv.D = D;
   sv.batch = c->batch;

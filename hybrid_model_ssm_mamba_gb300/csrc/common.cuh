@@ -35,6 +35,8 @@ struct StoreView {
   int4* meta;     // [batch] {start, n, pending, 0}
   int* arrive;    // [batch]
   int* status;
+  int4* plan;     // [batch] {start, n, kind, 0} of the step in flight
+  float* coef;    // [batch][H][cap + 1]
   const float* A;
   const float* D;
   int batch, H, G, hpg, L, cap;
@@ -329,14 +331,20 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
+// Programmatic dependent launch: a primary kernel lets its dependent start early; the
+// dependent waits, where it first needs the primary's results, until the primary grid has
+// completed and its writes are visible. Without the launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // Last-CTA-done update of a sequence's metadata: every CTA of sequence b calls this once,
 // from its single reader thread, after the value it read from meta[b] has been consumed
 // (written to shared memory and past a CTA barrier), so its read is complete; the last of
 // the H arrivals writes the new value and re-arms the counter. The new value is only read
 // by later launches. Nothing waits, so nothing can hang.
-__device__ __forceinline__ void arrive_and_publish(const StoreView& sv, int b, int4 next) {
+__device__ __forceinline__ void arrive_and_publish(const StoreView& sv, int b, int4 next, int count) {
   const int old = atomicAdd(&sv.arrive[b], 1);
-  if (old == sv.H - 1) {
+  if (old == count - 1) {
     sv.arrive[b] = 0;
     sv.meta[b] = next;
   }

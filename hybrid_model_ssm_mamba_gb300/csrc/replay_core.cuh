@@ -89,43 +89,6 @@ __device__ __forceinline__ void stage_records(const SlabRing<T>& ring, const Rin
         to_f(s < nring ? ring.dt[ring_slot(start, s, cap)] : ex.dt[(s - nring) * ex.dtstride]);
 }
 
-// Whole-ring image for the decode step: image slots 0..cap-1 hold a copy of the slab's ring
-// (x per head, B per group, dt) and slot cap holds the current token's record, so staging
-// needs no ring pointer and starts together with the checkpoint loads. Record s of the
-// window sits at image slot (start + s) mod cap for s < n and at slot cap for s == n.
-template <int P, int N, class T>
-__host__ __device__ constexpr size_t whole_image_bytes(int cap) {
-  return static_cast<size_t>(cap + 1) * (P + N) * sizeof(T) + static_cast<size_t>(cap + 1) * sizeof(float);
-}
-
-template <int P, int N, class T>
-__device__ __forceinline__ RingImage<T> whole_image(void* smem, int cap) {
-  RingImage<T> im;
-  im.x = static_cast<T*>(smem);
-  im.b = im.x + static_cast<size_t>(cap + 1) * P;
-  im.dt = reinterpret_cast<float*>(im.b + static_cast<size_t>(cap + 1) * N);
-  return im;
-}
-
-template <int P, int N, class T>
-__device__ __forceinline__ void stage_whole_ring(const SlabRing<T>& ring, const RingImage<T>& im, int cap,
-                                                 const T* xcur, const T* bcur, T dtcur) {
-  constexpr int EPC = 16 / sizeof(T);
-  constexpr int XC = P / EPC, BC = N / EPC;  // 16-byte chunks per record
-  const int nx = (cap + 1) * XC, total = nx + (cap + 1) * BC;
-  for (int c = threadIdx.x; c < total; c += kThreads) {
-    if (c < nx) {
-      const int s = c / XC, off = (c - s * XC) * EPC;
-      cp_async16(im.x + s * P + off, (s < cap ? ring.x + static_cast<size_t>(s) * P : xcur) + off);
-    } else {
-      const int c2 = c - nx;
-      const int s = c2 / BC, off = (c2 - s * BC) * EPC;
-      cp_async16(im.b + s * N + off, (s < cap ? ring.b + static_cast<size_t>(s) * N : bcur) + off);
-    }
-  }
-  for (int s = threadIdx.x; s <= cap; s += kThreads) im.dt[s] = to_f(s < cap ? ring.dt[s] : dtcur);
-}
-
 // Copy one record (x of this head, B of this group if `with_b`) from image slot `from` to
 // global ring slot `to` with 16-byte vectors, and dt from `dtv`.
 template <int P, int N, class T>

@@ -47,7 +47,7 @@ replay_fold_kernel(StoreView sv, float* __restrict__ out) {
   const ExtraRecords<T> none{nullptr, nullptr, nullptr, 0, 0, 0};
   stage_records<P, N, T>(ring, im, start, cap, n, n, none);
   if constexpr (MODE == 0) {
-    if (tid == 0) arrive_and_publish(sv, b, make_int4(ring_slot(start, n, cap), 0, 0, 0));
+    if (tid == 0) arrive_and_publish(sv, b, make_int4(ring_slot(start, n, cap), 0, 0, 0), sv.H);
   }
   cp_async_wait_all();
   __syncthreads();

@@ -9,11 +9,12 @@
 // keep the store (its workspace is memory they were given), but they cannot provide extra
 // memory for a kernel's scratch.
 //
-// replay_step's only scratch is its per-sequence arrival counter, which must read zero when
-// a launch starts. Here those counters live in a fixed array inside the library instead of
-// the store's `arrive` region: a file-scope device array of REPLAY_STATIC_MAX_BATCH ints that
-// every GPU loading the library holds until the process exits. The kernel and everything
-// else are replay_step's own.
+// replay_step's scratch is what it keeps only for the duration of one step: the
+// per-sequence arrival counters (which must read zero when a step starts), the step's plan
+// (the ring pointer it runs on) and the per-head record coefficients. Here all three live
+// in one fixed array inside the library instead of the store's arrive, plan and coef
+// regions: a file-scope device array that every GPU loading the library holds until the
+// process exits. The kernels and everything else are replay_step's own.
 #include <cstdint>
 #include <mutex>
 
@@ -22,24 +23,29 @@
 
 namespace {
 
-static __device__ __align__(256) int g_step_arrive_scratch[REPLAY_STATIC_MAX_BATCH];
+constexpr size_t kArriveBytes = sizeof(int) * REPLAY_STATIC_MAX_BATCH;
+constexpr size_t kPlanBytes = sizeof(int4) * REPLAY_STATIC_MAX_BATCH;
+constexpr size_t kCoefBytes = sizeof(float) * static_cast<size_t>(REPLAY_STATIC_MAX_COEFS);
+constexpr size_t kScratchBytes = kArriveBytes + kPlanBytes + kCoefBytes;
+
+static __device__ __align__(256) unsigned char g_step_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-int* g_scratch_ptr[kMaxDevices] = {};  // device address of the array, per device ordinal
+unsigned char* g_scratch_ptr[kMaxDevices] = {};  // device address of the array, per device
 
 // Device address of the scratch array on the current device, looked up once per device.
-// On the host, g_step_arrive_scratch names a host-side stand-in, never the device memory,
-// so the address must come from cudaGetSymbolAddress with that device current.
-int scratch_on_current_device(int** out) {
+// On the host, g_step_scratch names a host-side stand-in, never the device memory, so the
+// address must come from cudaGetSymbolAddress with that device current.
+int scratch_on_current_device(unsigned char** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return REPLAY_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return REPLAY_EUNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_step_arrive_scratch) != cudaSuccess || p == nullptr) return REPLAY_ECUDA;
-    g_scratch_ptr[dev] = static_cast<int*>(p);
+    if (cudaGetSymbolAddress(&p, g_step_scratch) != cudaSuccess || p == nullptr) return REPLAY_ECUDA;
+    g_scratch_ptr[dev] = static_cast<unsigned char*>(p);
   }
   *out = g_scratch_ptr[dev];
   return REPLAY_OK;
@@ -54,15 +60,20 @@ extern "C" int replay_step_static_scratch(replay_store* st, const void* x, const
   if (st == nullptr || x == nullptr || B == nullptr || C == nullptr || dt == nullptr || y == nullptr)
     return REPLAY_EBADARG;
   if (!aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
-  if (st->cfg.batch > REPLAY_STATIC_MAX_BATCH) return REPLAY_ECAPACITY;
-  int* scratch = nullptr;
+  const size_t coefs = static_cast<size_t>(st->cfg.batch) * st->cfg.nheads * (st->lay.cap + 1);
+  if (st->cfg.batch > REPLAY_STATIC_MAX_BATCH || coefs > static_cast<size_t>(REPLAY_STATIC_MAX_COEFS))
+    return REPLAY_ECAPACITY;
+  unsigned char* scratch = nullptr;
   int rc = scratch_on_current_device(&scratch);
   if (rc != REPLAY_OK) return rc;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps whatever the previous call left; the counters must start at zero.
+  // The array keeps whatever the previous call left: the arrival counters must start at
+  // zero (plan and coefficients are written by the step before they are read).
   if (cudaMemsetAsync(scratch, 0, sizeof(int) * static_cast<size_t>(st->cfg.batch), s) != cudaSuccess)
     return REPLAY_ECUDA;
   rssm::StoreView sv = st->sv;
-  sv.arrive = scratch;
+  sv.arrive = reinterpret_cast<int*>(scratch);
+  sv.plan = reinterpret_cast<int4*>(scratch + kArriveBytes);
+  sv.coef = reinterpret_cast<float*>(scratch + kArriveBytes + kPlanBytes);
   return rssm::launch_step(sv, st->sh, x, B, C, dt, y, s);
 }

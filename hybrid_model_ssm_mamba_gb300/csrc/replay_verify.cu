@@ -71,7 +71,7 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
   const ExtraRecords<T> drafts{x + xoff(0), B + boff(0), dt + doff(0), static_cast<size_t>(H) * P,
                                static_cast<size_t>(G) * N, static_cast<size_t>(H)};
   stage_records<P, N, T>(ring, im, start, cap, n + TT, n, drafts);
-  if (tid == 0) arrive_and_publish(sv, b, make_int4(start2, n2, TT, 0));
+  if (tid == 0) arrive_and_publish(sv, b, make_int4(start2, n2, TT, 0), H);
   if constexpr (RC != REPLAY_RC_NONE) {
     if (prefold) load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
   }

@@ -33,6 +33,7 @@ REPLAY_F32, REPLAY_BF16 = 0, 1
 REPLAY_RC_NONE, REPLAY_RC_BF16, REPLAY_RC_FP8E4M3 = 0, 1, 2
 REPLAY_DEV_BAD_META, REPLAY_DEV_BAD_ACCEPT = 1, 2
 REPLAY_STATIC_MAX_BATCH = 4096
+REPLAY_STATIC_MAX_COEFS = 1048576
 _ERRORS = {-1: "bad argument", -2: "unsupported shape or dtype", -3: "capacity exceeded",
            -4: "CUDA error"}
 
@@ -59,7 +60,8 @@ class ReplayConfig(ctypes.Structure):
 
 class ReplayLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "h0", "rc", "scale", "xbuf", "bbuf", "dtbuf", "meta", "arrive", "status", "total")] + \
+        "h0", "rc", "scale", "xbuf", "bbuf", "dtbuf", "meta", "arrive", "status", "plan", "coef",
+        "total")] + \
         [("cap", ctypes.c_int)]
 
 
@@ -293,6 +295,7 @@ class ReplayStore:
             "scale": (torch.float32, (Bz, H) if c.read_copy == REPLAY_RC_FP8E4M3 else (0,)),
             "xbuf": (dt, (Bz, H, cap, P)), "bbuf": (dt, (Bz, G, cap, N)), "dtbuf": (dt, (Bz, H, cap)),
             "meta": (torch.int32, (Bz, 4)), "arrive": (torch.int32, (Bz,)), "status": (torch.int32, (1,)),
+            "plan": (torch.int32, (Bz, 4)), "coef": (torch.float32, (Bz, H, cap + 1)),
         }[name]
         tdt, shape = spec
         nbytes = torch.empty((), dtype=tdt).element_size()

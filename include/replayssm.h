@@ -91,11 +91,13 @@ typedef struct replay_config {
  *          (start + s) mod cap, s < n; `pending` drafts sit beyond them after a verify
  *   arrive per sequence int32 counter (internal; zero between calls)
  *   status int32 device status word (REPLAY_DEV_* bits)
+ *   plan   per sequence int32 x4      (internal, per step: the pointer the step runs on)
+ *   coef   FP32 [batch][H][cap+1]     (internal, per step: record weights and decay)
  * cap = window_L when max_draft_T == 0, else window_L + 2*max_draft_T - 1: the most
  * records a sequence can hold (window_L - 1 + T committed before a verify folds them)
  * plus T drafts written beyond them while those are being folded. */
 typedef struct replay_layout {
-  size_t h0, rc, scale, xbuf, bbuf, dtbuf, meta, arrive, status;
+  size_t h0, rc, scale, xbuf, bbuf, dtbuf, meta, arrive, status, plan, coef;
   size_t total;  /* workspace bytes */
   int cap;       /* ring capacity in records */
 } replay_layout;
@@ -175,14 +177,15 @@ int replay_status(replay_store* st, int* status_out, int clear, void* stream);
  * Who needs it: callers that cannot call cudaMalloc (or anything that allocates) when they
  * decode -- an engine plugin handed only its input, output and state buffers, a process
  * whose device memory is pre-claimed by another framework's pool, code running while a
- * stream is captured. replay_step's one piece of scratch memory is a per-sequence arrival
- * counter; this call keeps those counters in a fixed array inside the library (the store's
- * `arrive` region is not touched) and is otherwise replay_step: same arguments, kernel,
- * results and errors.
+ * stream is captured. replay_step's scratch memory -- the per-sequence arrival counters, the
+ * step's plan and the per-head record coefficients, all only alive during one step -- is kept
+ * by this call in a fixed array inside the library (the store's arrive, plan and coef regions
+ * are not touched); otherwise it is replay_step: same arguments, kernels, results, errors.
  * Limits and rules:
- *  - batch <= REPLAY_STATIC_MAX_BATCH, else REPLAY_ECAPACITY and nothing is launched. The
- *    array (REPLAY_STATIC_MAX_BATCH int32, 16 KiB) exists on every GPU that loads the
- *    library, until the process exits.
+ *  - batch <= REPLAY_STATIC_MAX_BATCH and batch * nheads * (cap + 1) <= REPLAY_STATIC_MAX_COEFS
+ *    (cap: replay_layout), else REPLAY_ECAPACITY and nothing is launched. The array
+ *    (16 KiB of counters, 64 KiB of plans, 4 MiB of coefficients) exists on every GPU that
+ *    loads the library, until the process exits.
  *  - The first call on a device looks up the array's device address (once per device, with
  *    that device current); make that first call before any stream capture.
  *  - Each call zeroes the counters it uses (an asynchronous memset on `stream`, no
@@ -190,6 +193,7 @@ int replay_status(replay_store* st, int* status_out, int clear, void* stream);
  *    device that can overlap on the GPU (different streams, no ordering between them) race
  *    and give wrong results: order them, or use replay_step. */
 #define REPLAY_STATIC_MAX_BATCH 4096
+#define REPLAY_STATIC_MAX_COEFS 1048576
 int replay_step_static_scratch(replay_store* st, const void* x, const void* B, const void* C,
                                const void* dt, float* y, void* stream);
 

@@ -2,8 +2,8 @@
 
 Some callers cannot allocate when they decode (an engine plugin given only its buffers,
 memory pre-claimed by another framework's pool, code under stream capture). For them,
-replay_step_static_scratch keeps replay_step's only scratch -- the per-sequence arrival
-counters -- in a fixed array inside the library. These tests call it through the C ABI and
+replay_step_static_scratch keeps replay_step's per-step scratch -- arrival counters, plan,
+record coefficients -- in a fixed array inside the library. These tests call it through the C ABI and
 check it against replay_step on identical stores, call after call. This file is collected
 last on purpose, so a failing run has already run every other test.
 """
@@ -50,6 +50,17 @@ def test_matches_replay_step_on_consecutive_calls(lib):
         assert torch.equal(new.region("meta"), ref.region("meta")), t
     assert rel_vec_err(new.region("h0").cpu().numpy(), ref.region("h0").cpu().numpy(), 2).max() <= TOL
     assert new.status() == 0 and ref.status() == 0
+
+
+def test_rejects_more_coefficients_than_the_array_holds(lib):
+    shape = sg.LayerShape(128, 128, 64, 64, 1, "bf16")      # 128 * 128 * 65 > 2**20
+    st, _, _ = make_store(shape, 33, L=64)
+    assert shape.batch * shape.nheads * (st.layout.cap + 1) > R.REPLAY_STATIC_MAX_COEFS
+    devs, _ = step_inputs(shape, 33, 0)
+    y = torch.zeros(128, 128, 64, device="cuda")
+    assert _c_call(lib, st, devs, y) == -3
+    torch.cuda.synchronize()
+    assert not torch.any(y != 0)
 
 
 def test_rejects_batch_beyond_the_limit(lib):
