@@ -250,26 +250,55 @@ def run_replay(args, rank, world, local_rank):
     nf_s = launch_s[:, :-1].sum()
     traffic = recorded_traffic()
 
-    # e2e: inputs from pinned host memory, outputs back to pinned host memory, every token
+    # e2e: every token's inputs come from pinned host memory and its y goes back to pinned
+    # host memory, through the public call. Copies run on their own streams, double-buffered,
+    # so token t+1's inputs travel while token t decodes and y_t returns meanwhile.
     y_host = [torch.empty(w["batch"], w["nheads"], w["headdim"], pin_memory=True) for _ in range(L)]
-    stage = [[torch.empty_like(t) for t in ins] for ins in dev]
+    stage = [[torch.empty_like(t) for t in dev[0]] for _ in range(2)]
+    ybuf = [torch.empty_like(y) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
 
-    def e2e_window():
+    def e2e_window(prev):
+        """prev: events of the previous window's last two tokens (buffer reuse)."""
+        done_in, done_step, done_out = {}, dict(prev["step"]), dict(prev["out"])
         for t in range(L):
-            for dst, src in zip(stage[t], host[t]):
-                dst.copy_(src, non_blocking=True)
-            st.step(*stage[t], y)
-            y_host[t].copy_(y, non_blocking=True)
+            slot = t % 2
+            with torch.cuda.stream(s_in):
+                if (t - 2) in done_step:
+                    s_in.wait_event(done_step[t - 2])        # the step that read this buffer
+                for dst, src in zip(stage[slot], host[t]):
+                    dst.copy_(src, non_blocking=True)
+                done_in[t] = ev()
+                done_in[t].record(s_in)
+            stream.wait_event(done_in[t])
+            if (t - 2) in done_out:
+                stream.wait_event(done_out[t - 2])           # y buffer copied out
+            st.step(*stage[slot], ybuf[slot], stream)
+            done_step[t] = ev()
+            done_step[t].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_step[t])
+                y_host[t].copy_(ybuf[slot], non_blocking=True)
+                done_out[t] = ev()
+                done_out[t].record(s_out)
+        return {"step": {t - L: done_step[t] for t in (L - 2, L - 1)},
+                "out": {t - L: done_out[t] for t in (L - 2, L - 1)}}
 
+    prev = {"step": {}, "out": {}}
     for _ in range(2):
-        e2e_window()
+        prev = e2e_window(prev)
     e_steps = max(1, min(args.steps, 50))
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    s_in.wait_event(e0)
+    prev = {"step": {}, "out": {}}
     for _ in range(e_steps):
-        e2e_window()
+        prev = e2e_window(prev)
+    for e in prev["out"].values():
+        stream.wait_event(e)
     e1.record(stream)
     torch.cuda.synchronize()
     e_el = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, "cuda")
@@ -441,6 +470,88 @@ def run_read_copies(torch, R, dev, steps=10):
     return out
 
 
+def run_sweep(torch, R, tokens=512, distinct=32):
+    """Batch x window sweep on the tiny layer's shape (8 heads, FP32 inputs), replay vs the
+    conventional step, L2 flushed before every token (each token timed alone), plus a
+    40-layer stack at batch 256 (2.5 GiB of state, no flush needed). One JSON line each."""
+    out = []
+    shape_of = lambda b: sg.LayerShape(b, 8, 64, 128, 1, "f32")  # noqa: E731
+    A, D = sg.head_params(8, 0)
+    flush = l2_flusher(torch)
+
+    def inputs(b):
+        d = sg.token_inputs(shape_of(b), 0, np.arange(distinct))
+        return [[torch.from_numpy(np.ascontiguousarray(d[k].store[:, t])).cuda() for k in ("x", "B", "C", "dt")]
+                for t in range(distinct)]
+
+    def per_token_us(fn, n):
+        ev = []
+        for t in range(n):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn(t)
+            e1.record()
+            ev.append((e0, e1))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3
+
+    for b in (1, 16, 64, 256, 512):
+        ins = inputs(b)
+        y = torch.empty(b, 8, 64, device="cuda")
+        state = torch.zeros(b, 8, 64, 128, device="cuda")
+        cfg0 = R.ReplayConfig(b, 8, 64, 128, 1, 16, 0, R.REPLAY_F32, R.REPLAY_RC_NONE)
+        Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
+        conv = lambda t: R.conv_step(cfg0, state, R.REPLAY_F32, Ad, Dd, *ins[t % distinct], y)  # noqa: E731
+        conv(0)
+        c_us = per_token_us(conv, tokens)
+        for L in (4, 8, 16, 32):
+            cfg = R.ReplayConfig(b, 8, 64, 128, 1, L, 0, R.REPLAY_F32, R.REPLAY_RC_NONE)
+            st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
+            step = lambda t: st.step(*ins[t % distinct], y)  # noqa: E731
+            for t in range(L):
+                step(t)
+            r_us = per_token_us(step, tokens)
+            assert st.status() == 0
+            st.close()
+            out.append({"sweep": "tiny-layer shape, L2 flushed per token", "batch": b, "window_L": L,
+                        "tokens": tokens, "replay_us_per_token": r_us, "conv_us_per_token": c_us,
+                        "replay_tokens_per_s": b / (r_us * 1e-6), "conv_tokens_per_s": b / (c_us * 1e-6),
+                        "speedup": c_us / r_us})
+    # 40 independent layers at batch 256: every token runs all 40 layers' steps
+    b, layers, L = 256, 40, 16
+    ins = inputs(b)
+    y = torch.empty(b, 8, 64, device="cuda")
+    Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
+    cfg = R.ReplayConfig(b, 8, 64, 128, 1, L, 0, R.REPLAY_F32, R.REPLAY_RC_NONE)
+    stores = [R.ReplayStore(cfg, Ad, Dd) for _ in range(layers)]
+    states = [torch.zeros(b, 8, 64, 128, device="cuda") for _ in range(layers)]
+
+    def timed_stack(fn, n):
+        for t in range(L):
+            fn(t)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for t in range(n):
+            fn(t)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    r_stack = timed_stack(lambda t: [s.step(*ins[t % distinct], y) for s in stores], 64)
+    c_stack = timed_stack(lambda t: [R.conv_step(cfg, s, R.REPLAY_F32, Ad, Dd, *ins[t % distinct], y)
+                                     for s in states], 64)
+    for s in stores:
+        assert s.status() == 0
+        s.close()
+    out.append({"sweep": "40-layer stack, tiny-layer shape, batch 256, L 16 (2.5 GiB of state)",
+                "replay_us_per_token_all_layers": r_stack, "conv_us_per_token_all_layers": c_stack,
+                "replay_tokens_per_s": b / (r_stack * 1e-6), "conv_tokens_per_s": b / (c_stack * 1e-6),
+                "speedup": c_stack / r_stack})
+    return out
+
+
 # ------------------------------------------------------------------ the oracle (CPU)
 def oracle_tokens_per_s(n_seqs: int, n_tokens: int, seed: int = 0):
     """Time the FP64 oracle decoding n_tokens of n_seqs sequences of the workload (all
@@ -497,9 +608,19 @@ def main(argv=None):
     ap.add_argument("--cpu-sample-tokens", type=int, default=48)
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary workloads (read copies, speculative verify)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the benchmark line: batch x window sweep and 40-layer stack, "
+                         "one JSON line per configuration")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
     rank, world, local_rank = dist_env()
+    if args.sweep:
+        import torch
+        from hybrid_model_ssm_mamba_gb300 import replay as R
+        torch.cuda.set_device(local_rank)
+        for line in run_sweep(torch, R):
+            print(json.dumps(line), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
     else:

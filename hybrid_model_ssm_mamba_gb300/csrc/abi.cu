@@ -83,7 +83,7 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   L.arrive = take(Bn * 4);
   L.status = take(4);
   L.plan = take(Bn * 16);
-  L.coef = take(Bn * H * (cap + 1) * 4);
+  L.coef = take(Bn * H * (static_cast<size_t>(c->max_draft_T) + 1) * (cap + 1) * 4);
   L.total = off;
   *out = L;
   return REPLAY_OK;
@@ -130,6 +130,7 @@ int replay_alloc(const replay_config* c, void* workspace, size_t workspace_bytes
   sv.hpg = c->nheads / c->ngroups;
   sv.L = c->window_L;
   sv.cap = L.cap;
+  sv.tmax = c->max_draft_T;
   st->sh = rssm::Shape{c->headdim, c->dstate, c->in_dtype, c->read_copy};
   rc = replay_reset(st, nullptr, stream);
   if (rc != REPLAY_OK) {

@@ -39,7 +39,7 @@ struct StoreView {
   float* coef;    // [batch][H][cap + 1]
   const float* A;
   const float* D;
-  int batch, H, G, hpg, L, cap;
+  int batch, H, G, hpg, L, cap, tmax;
 };
 
 // ------------------------------------------------------------------ element conversion
@@ -314,6 +314,28 @@ __device__ __forceinline__ void load_rows(const T* p, float (&o)[RPW]) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[i + e] = t[e];
   }
+}
+
+// One 16-byte chunk (8 bf16 or 4 FP32 values) widened to float, and its FP32 store.
+template <class T>
+__device__ __forceinline__ void load16(const T* p, float (&o)[16 / sizeof(T)]) {
+  if constexpr (sizeof(T) == 4) {
+    ldv<4>(reinterpret_cast<const float*>(p), o);
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const unsigned w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      o[2 * i] = f.x;
+      o[2 * i + 1] = f.y;
+    }
+  }
+}
+template <int EPC>
+__device__ __forceinline__ void store16f(float* p, const float (&v)[EPC]) {
+#pragma unroll
+  for (int i = 0; i < EPC; i += 4) *reinterpret_cast<float4*>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
 }
 
 __device__ __forceinline__ int ring_slot(int start, int s, int cap) {

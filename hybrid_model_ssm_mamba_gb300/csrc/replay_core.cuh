@@ -258,4 +258,62 @@ __device__ __forceinline__ float* fold_staging(void* smem, size_t image_bytes) {
   return reinterpret_cast<float*>(static_cast<char*>(smem) + align128(image_bytes));
 }
 
+// Stage K records for a fold straight from global memory, in 16-byte chunks (all threads):
+// sm_u[s][p] = w[s] * x_s[p] and sm_b[s][c] = B_s[c] in FP32; x_of(s) and b_of(s) give the
+// record's x (this head) and B (this group). The caller puts a CTA barrier after it.
+template <int P, int N, class T, class XOf, class BOf>
+__device__ __forceinline__ void stage_weighted(XOf x_of, BOf b_of, const float* w, int K, float* sm_u,
+                                               float* sm_b) {
+  constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
+  for (int c = threadIdx.x; c < K * (XC + BC); c += kThreads) {
+    float v[EPC];
+    if (c < K * XC) {
+      const int s = c / XC, off = (c - s * XC) * EPC;
+      load16<T>(x_of(s) + off, v);
+      const float ws = w[s];
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) v[e] *= ws;
+      store16f<EPC>(sm_u + s * P + off, v);
+    } else {
+      const int c2 = c - K * XC;
+      const int s = c2 / BC, off = (c2 - s * BC) * EPC;
+      load16<T>(b_of(s) + off, v);
+      store16f<EPC>(sm_b + s * N + off, v);
+    }
+  }
+}
+
+// The rank-K update of a checkpoint tile from staged records: h <- gam * h + sum_s u_s B_s^T.
+template <int P, int N>
+__device__ __forceinline__ void fold_staged(const float* sm_u, const float* sm_b, int K, float gam,
+                                            float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+    for (int e = 0; e < TL::E; ++e) hv[i][e] *= gam;
+  for (int s = 0; s < K; ++s) {
+    float u[TL::RPW], bv[TL::E];
+    load_rows<TL::RPW>(sm_u + s * P + warp * TL::RPW, u);
+    load_cols<P, N>(sm_b + s * N, lane, bv);
+#pragma unroll
+    for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+      for (int e = 0; e < TL::E; ++e) hv[i][e] = fmaf(u[i], bv[e], hv[i][e]);
+  }
+}
+
+// Weights of a fold of K records for one head, written by one warp: w[s] for s < K and
+// Gamma_K at w[cap]. dt_of(s) gives record s's dt.
+template <class DtOf>
+__device__ __forceinline__ void write_fold_weights(DtOf dt_of, int K, float A, float* w, int cap, int lane) {
+  const float d0 = lane < K ? dt_of(lane) : 0.f;
+  const float d1 = lane + 32 < K ? dt_of(lane + 32) : 0.f;
+  const RecordWeights rw = record_weights(d0, d1, K, A, lane);
+  if (lane < K) w[lane] = rw.w0;
+  if (lane + 32 < K) w[lane + 32] = rw.w1;
+  if (lane == 0) w[cap] = rw.gam;
+}
+
 }  // namespace rssm

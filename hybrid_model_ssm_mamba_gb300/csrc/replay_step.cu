@@ -171,29 +171,10 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
     load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
   float* sm_u = reinterpret_cast<float*>(smem4);  // [k][P]: w_s x_s
   float* sm_b = sm_u + cap * P;                   // [k][N]: B_s
-  for (int idx = tid; idx < k * P; idx += kThreads) {
-    const int s = idx / P, p = idx - s * P;
-    sm_u[idx] = cf[s] * to_f(x_of(s)[p]);
-  }
-  for (int idx = tid; idx < k * N; idx += kThreads) {
-    const int s = idx / N, c = idx - s * N;
-    sm_b[idx] = to_f(s < n ? ring.b[static_cast<size_t>(ring_slot(start, s, cap)) * N + c] : B[bo + c]);
-  }
+  auto b_of = [&](int s) { return s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo; };
+  stage_weighted<P, N, T>(x_of, b_of, cf, k, sm_u, sm_b);
   __syncthreads();
-  const float gam = cf[cap];
-#pragma unroll
-  for (int i = 0; i < RPW; ++i)
-#pragma unroll
-    for (int e = 0; e < E; ++e) hv[i][e] *= gam;
-  for (int s = 0; s < k; ++s) {
-    float u[RPW], bv[E];
-    load_rows<RPW>(sm_u + s * P + warp * RPW, u);
-    load_cols<P, N>(sm_b + s * N, lane, bv);
-#pragma unroll
-    for (int i = 0; i < RPW; ++i)
-#pragma unroll
-      for (int e = 0; e < E; ++e) hv[i][e] = fmaf(u[i], bv[e], hv[i][e]);
-  }
+  fold_staged<P, N>(sm_u, sm_b, k, cf[cap], hv);
   float zero[RPW];
 #pragma unroll
   for (int i = 0; i < RPW; ++i) zero[i] = 0.f;

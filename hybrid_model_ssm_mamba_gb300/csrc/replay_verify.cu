@@ -9,17 +9,96 @@
 // output-only evaluation: the checkpoint is read once for all T queries and every other
 // term is a scalar (B_s . C_j, times a decay) scaling a cached x_s -- no state is formed.
 //
-// One CTA per (sequence, head) slab, as in the step kernel: the checkpoint tile is loaded
-// into registers first; the committed records and the drafts are staged in a shared-memory
-// image of the ring (the drafts at the slots they are appended to); when n >= L committed
-// records are waiting they are folded into the tile and written as the new checkpoint
-// before the drafts are evaluated.
+// Two kernels, as for the decode step.
+//  1. replay_verify_prep_kernel, one CTA per (sequence, group): reads the ring pointer,
+//     records the call's plan, publishes the next pointer (drafts pending beyond it),
+//     computes the B_s . C_j dots of the group once (s <= n + j: the committed records and
+//     the drafts up to j), and per head the fold weights of the committed records (when
+//     n >= L they are folded first) and the query coefficients
+//        c_j[s] = exp(A sum_{r=s+1..n+j} dt_r) dt_s (B_s . C_j),  Gamma_j = exp(A sum_{r<=n+j} dt_r).
+//  2. replay_verify_kernel, one CTA per (sequence, head) slab, a programmatic dependent of
+//     the prep: the checkpoint tile is loaded first; a pre-fold, when planned, stages and
+//     folds the committed records and writes the checkpoint; then for each draft j one warp
+//     reduction sums Gamma_j h0 . C_j and sum_s c_j[s] x_s (lane s carries record s). The
+//     drafts' records are appended beyond the committed ones.
 #include "launch.h"
 #include "replay_core.cuh"
 
 namespace rssm {
 
 constexpr int kMaxDrafts = 8;
+constexpr int kVerifyBad = -1, kVerifyPlain = 0, kVerifyPrefold = 1;
+
+template <int P, int N, class T>
+__global__ void __launch_bounds__(kThreads)
+replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T* __restrict__ C,
+                          const T* __restrict__ dt) {
+  using TL = Tile<P, N>;
+  __shared__ int4 s_meta;
+  __shared__ float s_bc[kMaxDrafts][kMaxCap];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.x, b = blockIdx.y;
+  const int H = sv.H, G = sv.G, cap = sv.cap;
+  auto boff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * G * N + static_cast<size_t>(g) * N; };
+  griddep_launch_dependents();  // the head CTAs may start their checkpoint loads now
+  if (tid == 0) s_meta = sv.meta[b];
+  __syncthreads();
+  const int start = s_meta.x, n = s_meta.y;
+  if (n < 0 || start < 0 || start >= cap || n + TT > cap) {
+    if (tid == 0) {
+      if (g == 0) sv.plan[b] = make_int4(start, n, kVerifyBad, 0);
+      set_status(sv.status, REPLAY_DEV_BAD_META);
+    }
+    return;
+  }
+  const bool prefold = n >= sv.L;
+  const int start2 = prefold ? ring_slot(start, n, cap) : start;
+  const int n2 = prefold ? 0 : n;
+  if (tid == 0) {
+    if (g == 0) sv.plan[b] = make_int4(start, n, prefold ? kVerifyPrefold : kVerifyPlain, 0);
+    arrive_and_publish(sv, b, make_int4(start2, n2, TT, 0), G);
+  }
+  const T* bring = static_cast<const T*>(sv.bbuf) + (static_cast<size_t>(b) * G + g) * cap * N;
+  const int kk = n2 + TT;  // committed records after any pre-fold, then the drafts
+  for (int pi = warp; pi < TT * kk; pi += kWarps) {
+    const int j = pi / kk, s = pi - j * kk;
+    if (s > n2 + j) continue;
+    float bv[TL::E], cj[TL::E];
+    load_cols<P, N>(s < n2 ? bring + static_cast<size_t>(ring_slot(start2, s, cap)) * N : B + boff(s - n2), lane, bv);
+    load_cols<P, N>(C + boff(j), lane, cj);
+    float d = 0.f;
+#pragma unroll
+    for (int e = 0; e < TL::E; ++e) d = fmaf(bv[e], cj[e], d);
+    d = warp_sum(d);
+    if (lane == 0) s_bc[j][s] = d;
+  }
+  __syncthreads();
+  const int cs = cap + 1;
+  for (int hh = warp; hh < sv.hpg; hh += kWarps) {
+    const int h = g * sv.hpg + hh;
+    const size_t slab = static_cast<size_t>(b) * H + h;
+    const float A = sv.A[h];
+    const T* dtr = static_cast<const T*>(sv.dtbuf) + slab * cap;
+    float* cf = sv.coef + slab * (sv.tmax + 1) * cs;
+    if (prefold) {
+      auto dt_fold = [&](int s) { return to_f(dtr[ring_slot(start, s, cap)]); };
+      write_fold_weights(dt_fold, n, A, cf, cap, lane);
+    }
+    auto dt_q = [&](int s) {
+      return to_f(s < n2 ? dtr[ring_slot(start2, s, cap)] : dt[(static_cast<size_t>(b) * TT + (s - n2)) * H + h]);
+    };
+    const float d0 = lane < kk ? dt_q(lane) : 0.f;
+    const float d1 = lane + 32 < kk ? dt_q(lane + 32) : 0.f;
+    for (int j = 0; j < TT; ++j) {
+      const int k = n2 + j + 1;
+      const RecordWeights rw = record_weights(lane < k ? d0 : 0.f, lane + 32 < k ? d1 : 0.f, k, A, lane);
+      float* cj = cf + (1 + j) * cs;
+      if (lane < k) cj[lane] = rw.w0 * s_bc[j][lane];
+      if (lane + 32 < k) cj[lane + 32] = rw.w1 * s_bc[j][lane + 32];
+      if (lane == 0) cj[cap] = rw.gam;
+    }
+  }
+}
 
 template <int P, int N, class T, int RC>
 __global__ void __launch_bounds__(kThreads, kMinBlocks<N> == 4 ? 3 : 2)
@@ -27,24 +106,19 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
                      const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
   using TL = Tile<P, N>;
   constexpr int RPW = TL::RPW, E = TL::E;
+  constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
   extern __shared__ float4 smem4[];
-  __shared__ int4 s_meta;
-  __shared__ float s_bc[kMaxDrafts][kMaxCap];
-  __shared__ float s_w[kMaxCap + 1];
   __shared__ float s_red[kWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int H = sv.H, G = sv.G;
+  const int H = sv.H, G = sv.G, cap = sv.cap;
   const int g = blockIdx.y, b = blockIdx.z;
   const int h = g * sv.hpg + blockIdx.x;
   const int slab = b * H + h;
-  const int cap = sv.cap;
   // draft j of sequence b: x/y at ((b*TT + j)*H + h)*P, B/C at ((b*TT + j)*G + g)*N
   auto xoff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * H * P + static_cast<size_t>(h) * P; };
   auto boff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * G * N + static_cast<size_t>(g) * N; };
-  auto doff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * H + h; };
 
-  if (tid == 0) s_meta = sv.meta[b];
   float hv[RPW][E];
   if constexpr (RC == REPLAY_RC_NONE) {
     load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
@@ -53,96 +127,99 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
     load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv);
   }
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
-  const float A = sv.A[h], Dh = sv.D[h];
-  __syncthreads();
+  const float Dh = sv.D[h];
 
-  const int start = s_meta.x, n = s_meta.y;
-  if (n < 0 || start < 0 || start >= cap || n + TT > cap) {
+  griddep_wait();  // plan and coefficients of this call are written
+  const int4 pl = sv.plan[b];
+  if (pl.z == kVerifyBad) {
     for (int j = 0; j < TT; ++j)
       if (tid < P) y[xoff(j) + tid] = __int_as_float(0x7fc00000);
-    if (tid == 0) set_status(sv.status, REPLAY_DEV_BAD_META);
     return;
   }
-  const bool prefold = n >= sv.L;  // fold the committed records first (flush of committed only)
+  const int start = pl.x, n = pl.y;
+  const bool prefold = pl.z == kVerifyPrefold;
   const int start2 = prefold ? ring_slot(start, n, cap) : start;
   const int n2 = prefold ? 0 : n;
+  const int cs = cap + 1;
+  const float* cf = sv.coef + static_cast<size_t>(slab) * (sv.tmax + 1) * cs;
   const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
-  const RingImage<T> im = ring_image<P, N, T>(smem4, cap);
-  const ExtraRecords<T> drafts{x + xoff(0), B + boff(0), dt + doff(0), static_cast<size_t>(H) * P,
-                               static_cast<size_t>(G) * N, static_cast<size_t>(H)};
-  stage_records<P, N, T>(ring, im, start, cap, n + TT, n, drafts);
-  if (tid == 0) arrive_and_publish(sv, b, make_int4(start2, n2, TT, 0), H);
-  if constexpr (RC != REPLAY_RC_NONE) {
-    if (prefold) load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
-  }
-  cp_async_wait_all();
-  __syncthreads();
 
-  if (prefold) {
-    auto slot_of = [&](int s) { return ring_slot(start, s, cap); };
-    float* sm_u = fold_staging(smem4, ring_image_bytes<P, N, T>(cap));
-    fold_tile<P, N, T>(im, slot_of, n, A, sm_u, sm_u + cap * P, s_w, hv);
+  if (prefold) {  // a flush of the committed records, from the FP32 checkpoint
+    if constexpr (RC != REPLAY_RC_NONE)
+      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    float* sm_u = reinterpret_cast<float*>(smem4);
+    float* sm_b = sm_u + cap * P;
+    auto xf = [&](int s) { return ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P; };
+    auto bf = [&](int s) { return ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N; };
+    stage_weighted<P, N, T>(xf, bf, cf, n, sm_u, sm_b);
+    __syncthreads();
+    fold_staged<P, N>(sm_u, sm_b, n, cf[cap], hv);
     write_checkpoint<P, N, RC>(sv, slab, s_red, hv);
   }
-  const int kk = n2 + TT;  // committed records, then the drafts, from slot start2
-  // B_s . C_j for every record s a draft j sees (s <= n2 + j); the pair loop is warp-strided
-  for (int pi = warp; pi < TT * kk; pi += kWarps) {
-    const int j = pi / kk, s = pi - j * kk;
-    if (s > n2 + j) continue;
-    float bv[E], cj[E];
-    load_cols<P, N>(im.b + ring_slot(start2, s, cap) * N, lane, bv);
-    load_cols<P, N>(C + boff(j), lane, cj);
-    float d = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) d = fmaf(bv[e], cj[e], d);
-    d = warp_sum(d);
-    if (lane == 0) s_bc[j][s] = d;
-  }
-  __syncthreads();
 
+  const int kk = n2 + TT;
+  auto x_of = [&](int s) {
+    return s < n2 ? ring.x + static_cast<size_t>(ring_slot(start2, s, cap)) * P : x + xoff(s - n2);
+  };
   float xr0[RPW], xr1[RPW];  // records lane and lane + 32: x values of this warp's rows
 #pragma unroll
   for (int i = 0; i < RPW; ++i) xr0[i] = xr1[i] = 0.f;
-  if (lane < kk) load_rows<RPW>(im.x + ring_slot(start2, lane, cap) * P + warp * RPW, xr0);
-  if (lane + 32 < kk) load_rows<RPW>(im.x + ring_slot(start2, lane + 32, cap) * P + warp * RPW, xr1);
-  const float dt0 = lane < kk ? im.dt[ring_slot(start2, lane, cap)] : 0.f;
-  const float dt1 = lane + 32 < kk ? im.dt[ring_slot(start2, lane + 32, cap)] : 0.f;
+  if (lane < kk) load_rows<RPW>(x_of(lane) + warp * RPW, xr0);
+  if (lane + 32 < kk) load_rows<RPW>(x_of(lane + 32) + warp * RPW, xr1);
   for (int j = 0; j < TT; ++j) {
     const int k = n2 + j + 1;  // records draft j sees, itself included
-    const RecordWeights rw = record_weights(lane < k ? dt0 : 0.f, lane + 32 < k ? dt1 : 0.f, k, A, lane);
-    const float c0 = lane < k ? rw.w0 * s_bc[j][lane] : 0.f;
-    const float c1 = lane + 32 < k ? rw.w1 * s_bc[j][lane + 32] : 0.f;
+    const float* cj = cf + (1 + j) * cs;
+    const float c0 = lane < k ? cj[lane] : 0.f;
+    const float c1 = lane + 32 < k ? cj[lane + 32] : 0.f;
     float ex[RPW];
 #pragma unroll
     for (int i = 0; i < RPW; ++i) ex[i] = fmaf(c1, xr1[i], c0 * xr0[i]);
     float cq[E];
     load_cols<P, N>(C + boff(j), lane, cq);
-    const float sum = tile_rows_dot<P, N>(hv, cq, rw.gam, ex, lane);
-    if (transpose_leader<RPW>(lane)) {
-      const float xj = to_f(im.x[ring_slot(start2, n2 + j, cap) * P + myrow]);
-      y[xoff(j) + myrow] = fmaf(Dh, xj, sum);
-    }
+    const float sum = tile_rows_dot<P, N>(hv, cq, cj[cap], ex, lane);
+    if (transpose_leader<RPW>(lane)) y[xoff(j) + myrow] = fmaf(Dh, to_f(x[xoff(j) + myrow]), sum);
   }
   // the drafts' records go to the ring beyond the committed ones; the pointer stays
   for (int j = 0; j < TT; ++j) {
     const int slot = ring_slot(start2, n2 + j, cap);
-    append_record<P, N, T>(ring, im, slot, slot, blockIdx.x == 0, dt[doff(j)]);
+    if (tid < XC) {
+      *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
+          *reinterpret_cast<const uint4*>(x + xoff(j) + tid * EPC);
+    } else if (blockIdx.x == 0 && tid < XC + BC) {
+      const int c = tid - XC;
+      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+          *reinterpret_cast<const uint4*>(B + boff(j) + c * EPC);
+    } else if (tid == XC + BC) {
+      ring.dt[slot] = dt[(static_cast<size_t>(b) * TT + j) * H + h];
+    }
   }
 }
 
 template <int P, int N, class T, int RC>
 static int launch(const StoreView& sv, int TT, const void* x, const void* B, const void* C,
                   const void* dt, float* y, cudaStream_t stream) {
+  replay_verify_prep_kernel<P, N, T><<<dim3(sv.G, sv.batch), kThreads, 0, stream>>>(
+      sv, TT, static_cast<const T*>(B), static_cast<const T*>(C), static_cast<const T*>(dt));
+  if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
   auto kern = replay_verify_kernel<P, N, T, RC>;
-  const size_t smem = smem_plan_bytes<P, N>(ring_image_bytes<P, N, T>(sv.cap), sv.cap);
+  const size_t smem = fold_staging_bytes<P, N>(sv.cap);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
-  const dim3 grid(sv.hpg, sv.G, sv.batch);
-  kern<<<grid, kThreads, smem, stream>>>(sv, TT, static_cast<const T*>(x), static_cast<const T*>(B),
-                                         static_cast<const T*>(C), static_cast<const T*>(dt), y);
-  return cudaGetLastError() == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sv.hpg, sv.G, sv.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, sv, TT, static_cast<const T*>(x), static_cast<const T*>(B),
+                                           static_cast<const T*>(C), static_cast<const T*>(dt), y);
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA;
 }
 
 int launch_verify(const StoreView& sv, const Shape& sh, int T, const void* x, const void* B,

@@ -92,7 +92,8 @@ typedef struct replay_config {
  *   arrive per sequence int32 counter (internal; zero between calls)
  *   status int32 device status word (REPLAY_DEV_* bits)
  *   plan   per sequence int32 x4      (internal, per step: the pointer the step runs on)
- *   coef   FP32 [batch][H][cap+1]     (internal, per step: record weights and decay)
+ *   coef   FP32 [batch][H][T+1][cap+1] (internal, per call: record weights and decays;
+ *          T = max_draft_T; a step uses block 0, a verify blocks 0..T)
  * cap = window_L when max_draft_T == 0, else window_L + 2*max_draft_T - 1: the most
  * records a sequence can hold (window_L - 1 + T committed before a verify folds them)
  * plus T drafts written beyond them while those are being folded. */
