@@ -58,12 +58,23 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
   }
   const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
   if (!flush) {
+    // stage the k records' B and this token's C in shared memory (one round trip)
+    extern __shared__ float4 smem4[];
+    T* sb = reinterpret_cast<T*>(smem4);  // [k][N] B, then [N] C
     const T* bring = static_cast<const T*>(sv.bbuf) + (static_cast<size_t>(b) * sv.G + g) * cap * N;
+    constexpr int EPC = 16 / sizeof(T), BC = N / EPC;
+    for (int c = tid; c < (k + 1) * BC; c += kThreads) {
+      const int r = c / BC, off = (c - r * BC) * EPC;
+      const T* src = r == k ? C + bo : (r < n ? bring + static_cast<size_t>(ring_slot(start, r, cap)) * N : B + bo);
+      cp_async16(sb + static_cast<size_t>(r) * N + off, src + off);
+    }
+    cp_async_wait_all();
+    __syncthreads();
     float cv[TL::E];
-    load_cols<P, N>(C + bo, lane, cv);
+    load_cols<P, N>(sb + static_cast<size_t>(k) * N, lane, cv);
     for (int s = warp; s < k; s += kWarps) {
       float bv[TL::E];
-      load_cols<P, N>(s < n ? bring + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo, lane, bv);
+      load_cols<P, N>(sb + static_cast<size_t>(s) * N, lane, bv);
       float d = 0.f;
 #pragma unroll
       for (int e = 0; e < TL::E; ++e) d = fmaf(bv[e], cv[e], d);
@@ -186,8 +197,14 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
 template <int P, int N, class T, int RC>
 static int launch(const StoreView& sv, const void* x, const void* B, const void* C, const void* dt,
                   float* y, cudaStream_t stream) {
-  replay_step_prep_kernel<P, N, T><<<dim3(sv.G, sv.batch), kThreads, 0, stream>>>(
-      sv, static_cast<const T*>(B), static_cast<const T*>(C), static_cast<const T*>(dt));
+  auto prep = replay_step_prep_kernel<P, N, T>;
+  const size_t psmem = static_cast<size_t>(sv.cap + 1) * N * sizeof(T);
+  if (psmem > 48 * 1024 &&
+      cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
+          cudaSuccess)
+    return REPLAY_ECUDA;
+  prep<<<dim3(sv.G, sv.batch), kThreads, psmem, stream>>>(sv, static_cast<const T*>(B), static_cast<const T*>(C),
+                                                          static_cast<const T*>(dt));
   if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
   auto kern = replay_step_kernel<P, N, T, RC>;
   const size_t smem = fold_staging_bytes<P, N>(sv.cap);

@@ -60,12 +60,26 @@ replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T
   }
   const T* bring = static_cast<const T*>(sv.bbuf) + (static_cast<size_t>(b) * G + g) * cap * N;
   const int kk = n2 + TT;  // committed records after any pre-fold, then the drafts
+  // stage the kk records' B and the TT queries' C in shared memory (one round trip)
+  extern __shared__ float4 smem4[];
+  T* sb = reinterpret_cast<T*>(smem4);  // [kk][N] B of the records, then [TT][N] C of the drafts
+  {
+    constexpr int EPC = 16 / sizeof(T), BC = N / EPC;
+    for (int c = tid; c < (kk + TT) * BC; c += kThreads) {
+      const int r = c / BC, off = (c - r * BC) * EPC;
+      const T* src = r >= kk ? C + boff(r - kk)
+                             : (r < n2 ? bring + static_cast<size_t>(ring_slot(start2, r, cap)) * N : B + boff(r - n2));
+      cp_async16(sb + static_cast<size_t>(r) * N + off, src + off);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+  }
   for (int pi = warp; pi < TT * kk; pi += kWarps) {
     const int j = pi / kk, s = pi - j * kk;
     if (s > n2 + j) continue;
     float bv[TL::E], cj[TL::E];
-    load_cols<P, N>(s < n2 ? bring + static_cast<size_t>(ring_slot(start2, s, cap)) * N : B + boff(s - n2), lane, bv);
-    load_cols<P, N>(C + boff(j), lane, cj);
+    load_cols<P, N>(sb + static_cast<size_t>(s) * N, lane, bv);
+    load_cols<P, N>(sb + static_cast<size_t>(kk + j) * N, lane, cj);
     float d = 0.f;
 #pragma unroll
     for (int e = 0; e < TL::E; ++e) d = fmaf(bv[e], cj[e], d);
@@ -128,8 +142,23 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
   }
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
   const float Dh = sv.D[h];
+  // the drafts' C (this group) and x (this head), staged while the prep kernel runs
+  T* sq = reinterpret_cast<T*>(reinterpret_cast<char*>(smem4) + fold_staging_bytes<P, N>(cap));
+  T* sx = sq + static_cast<size_t>(TT) * N;
+  for (int c = tid; c < TT * (BC + XC); c += kThreads) {
+    if (c < TT * BC) {
+      const int j = c / BC, off = (c - j * BC) * EPC;
+      cp_async16(sq + j * N + off, C + boff(j) + off);
+    } else {
+      const int c2 = c - TT * BC;
+      const int j = c2 / XC, off = (c2 - j * XC) * EPC;
+      cp_async16(sx + j * P + off, x + xoff(j) + off);
+    }
+  }
 
   griddep_wait();  // plan and coefficients of this call are written
+  cp_async_wait_all();
+  __syncthreads();
   const int4 pl = sv.plan[b];
   if (pl.z == kVerifyBad) {
     for (int j = 0; j < TT; ++j)
@@ -175,9 +204,9 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
 #pragma unroll
     for (int i = 0; i < RPW; ++i) ex[i] = fmaf(c1, xr1[i], c0 * xr0[i]);
     float cq[E];
-    load_cols<P, N>(C + boff(j), lane, cq);
+    load_cols<P, N>(sq + j * N, lane, cq);
     const float sum = tile_rows_dot<P, N>(hv, cq, cj[cap], ex, lane);
-    if (transpose_leader<RPW>(lane)) y[xoff(j) + myrow] = fmaf(Dh, to_f(x[xoff(j) + myrow]), sum);
+    if (transpose_leader<RPW>(lane)) y[xoff(j) + myrow] = fmaf(Dh, to_f(sx[j * P + myrow]), sum);
   }
   // the drafts' records go to the ring beyond the committed ones; the pointer stays
   for (int j = 0; j < TT; ++j) {
@@ -198,11 +227,17 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
 template <int P, int N, class T, int RC>
 static int launch(const StoreView& sv, int TT, const void* x, const void* B, const void* C,
                   const void* dt, float* y, cudaStream_t stream) {
-  replay_verify_prep_kernel<P, N, T><<<dim3(sv.G, sv.batch), kThreads, 0, stream>>>(
-      sv, TT, static_cast<const T*>(B), static_cast<const T*>(C), static_cast<const T*>(dt));
+  auto prep = replay_verify_prep_kernel<P, N, T>;
+  const size_t psmem = static_cast<size_t>(sv.cap + kMaxDrafts) * N * sizeof(T);
+  if (psmem > 48 * 1024 &&
+      cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
+          cudaSuccess)
+    return REPLAY_ECUDA;
+  prep<<<dim3(sv.G, sv.batch), kThreads, psmem, stream>>>(sv, TT, static_cast<const T*>(B),
+                                                          static_cast<const T*>(C), static_cast<const T*>(dt));
   if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
   auto kern = replay_verify_kernel<P, N, T, RC>;
-  const size_t smem = fold_staging_bytes<P, N>(sv.cap);
+  const size_t smem = fold_staging_bytes<P, N>(sv.cap) + static_cast<size_t>(TT) * (P + N) * sizeof(T);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
