@@ -43,12 +43,13 @@ def record_bytes(w, esz):
     return (w["nheads"] * w["headdim"] + w["ngroups"] * w["dstate"] + w["nheads"]) * esz
 
 
-def step_bytes(w, n_prior: int, flush: bool, esz=2, state_bytes=4, rc_bytes=0):
+def step_bytes(w, n_prior: int, flush: bool, esz=2, state_bytes=4, rc_bytes=0, shared=False):
     """Algorithmic HBM bytes of one replay_step launch over the batch.
 
     Reads: the checkpoint (FP32, or the read copy on a non-flush step), the n_prior
     buffered records, this token's inputs (x, B, C, dt). Writes: y (FP32) and either the
-    appended record (non-flush) or the new checkpoint (+ read copy) (flush).
+    appended record (non-flush) or the new checkpoint (+ read copy) (flush). With a shared
+    checkpoint the copy is the only state: a flush reads and writes just the copy.
     """
     b, H, P, N, G = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
     S = b * H * P * N
@@ -56,8 +57,10 @@ def step_bytes(w, n_prior: int, flush: bool, esz=2, state_bytes=4, rc_bytes=0):
     inputs = b * (H * P + 2 * G * N + H) * esz
     y = b * H * P * 4
     if flush:
-        return S * state_bytes + n_prior * rec + inputs + y + S * (state_bytes + rc_bytes) + \
-            (b * H * 4 if rc_bytes == 1 else 0)
+        scale = b * H * 4 if rc_bytes == 1 else 0
+        if shared:
+            return 2 * (S * rc_bytes + scale) + n_prior * rec + inputs + y
+        return S * state_bytes + n_prior * rec + inputs + y + S * (state_bytes + rc_bytes) + scale
     read = S * (rc_bytes if rc_bytes else state_bytes) + (b * H * 4 if rc_bytes == 1 else 0)
     return read + n_prior * rec + inputs + y + rec
 
@@ -435,15 +438,19 @@ def run_speculative(torch, R, calls=64, distinct=16):
 
 
 def run_read_copies(torch, R, dev, steps=10):
-    """The headline window with a bf16 and with an E4M3 read copy of the checkpoint."""
+    """The headline window with a bf16, E4M3 or FP16 read copy of the FP32 checkpoint, and
+    with a shared bf16, E4M3 or FP16 (stochastically rounded) checkpoint."""
     w = WORKLOAD
     L = w["L"]
     A, D = sg.head_params(w["nheads"], 0)
     y = torch.empty(w["batch"], w["nheads"], w["headdim"], device="cuda")
     out = {}
-    for name, rc, rcb in (("bf16", R.REPLAY_RC_BF16, 2), ("e4m3", R.REPLAY_RC_FP8E4M3, 1)):
+    for name, rc, rcb, shared in (("bf16", R.REPLAY_RC_BF16, 2, 0), ("e4m3", R.REPLAY_RC_FP8E4M3, 1, 0),
+                                  ("fp16", R.REPLAY_RC_FP16, 2, 0), ("shared_bf16", R.REPLAY_RC_BF16, 2, 1),
+                                  ("shared_e4m3", R.REPLAY_RC_FP8E4M3, 1, 1),
+                                  ("shared_fp16_sr", R.REPLAY_RC_FP16, 2, 1)):
         cfg = R.ReplayConfig(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], L, 0,
-                             R.REPLAY_BF16, rc)
+                             R.REPLAY_BF16, rc, shared)
         st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
         for _ in range(2):
             for t in range(L):
@@ -458,7 +465,7 @@ def run_read_copies(torch, R, dev, steps=10):
         torch.cuda.synchronize()
         us = np.array([a.elapsed_time(b) for a, b in ev]).reshape(steps, L) * 1e3
         nf_bytes = sum(step_bytes(w, t, False, rc_bytes=rcb) for t in range(L - 1))
-        fl_bytes = step_bytes(w, L - 1, True, rc_bytes=rcb)
+        fl_bytes = step_bytes(w, L - 1, True, rc_bytes=rcb, shared=bool(shared))
         out[name] = {"tokens_per_s": w["batch"] * L / (us.sum(axis=1).mean() * 1e-6),
                      "nonflush_launch_us": float(us[:, :-1].mean()),
                      "flush_launch_us": float(us[:, -1].mean()),

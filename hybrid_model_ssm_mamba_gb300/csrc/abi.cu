@@ -57,14 +57,17 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   int rc = check_shape(c);
   if (rc != REPLAY_OK) return rc;
   if (c->window_L < 1 || c->max_draft_T < 0) return REPLAY_EBADARG;
-  if (c->read_copy < REPLAY_RC_NONE || c->read_copy > REPLAY_RC_FP8E4M3) return REPLAY_EBADARG;
+  if (c->read_copy < REPLAY_RC_NONE || c->read_copy > REPLAY_RC_FP16) return REPLAY_EBADARG;
+  if (c->read_copy == REPLAY_RC_FP16 && c->dstate > 128) return REPLAY_EUNSUPPORTED;
+  if (c->shared_checkpoint != 0 && (c->shared_checkpoint != 1 || c->read_copy == REPLAY_RC_NONE))
+    return REPLAY_EBADARG;
   if (c->max_draft_T > 8) return REPLAY_ECAPACITY;
   const long long cap = c->max_draft_T > 0 ? static_cast<long long>(c->window_L) + 2LL * c->max_draft_T - 1
                                            : c->window_L;
   if (cap > rssm::kMaxCap) return REPLAY_ECAPACITY;
   const size_t Bn = c->batch, H = c->nheads, G = c->ngroups, P = c->headdim, N = c->dstate;
   const size_t esz = c->in_dtype == REPLAY_F32 ? 4 : 2;
-  const size_t rcsz = c->read_copy == REPLAY_RC_BF16 ? 2 : (c->read_copy == REPLAY_RC_FP8E4M3 ? 1 : 0);
+  const size_t rcsz = c->read_copy == REPLAY_RC_NONE ? 0 : (c->read_copy == REPLAY_RC_FP8E4M3 ? 1 : 2);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -73,7 +76,7 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   };
   replay_layout L;
   L.cap = static_cast<int>(cap);
-  L.h0 = take(Bn * H * P * N * 4);
+  L.h0 = take(c->shared_checkpoint ? 0 : Bn * H * P * N * 4);  // no FP32 checkpoint when shared
   L.rc = take(Bn * H * P * N * rcsz);
   L.scale = take(c->read_copy == REPLAY_RC_FP8E4M3 ? Bn * H * 4 : 0);
   L.xbuf = take(Bn * H * cap * P * esz);
@@ -131,6 +134,7 @@ int replay_alloc(const replay_config* c, void* workspace, size_t workspace_bytes
   sv.L = c->window_L;
   sv.cap = L.cap;
   sv.tmax = c->max_draft_T;
+  sv.shared = c->shared_checkpoint;
   st->sh = rssm::Shape{c->headdim, c->dstate, c->in_dtype, c->read_copy};
   rc = replay_reset(st, nullptr, stream);
   if (rc != REPLAY_OK) {

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -14,6 +15,7 @@ namespace rssm {
 constexpr int kThreads = 256;  // one CTA per (sequence, head) slab: 8 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCap = 64;    // ring records a sequence can hold (2 per lane)
+constexpr int kDtStage = 1024; // dt values a prep CTA stages in shared memory at once
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kE4M3Max = 448.0f;
 
@@ -27,12 +29,12 @@ using bf16 = __nv_bfloat16;
 // Everything a kernel needs to find a store's regions (passed by value).
 struct StoreView {
   float* h0;      // [batch][H][P][N]
-  void* rc;       // read copy, bf16 or e4m3 [batch][H][P][N]
+  void* rc;       // read copy, bf16, e4m3 or fp16 [batch][H][P][N]
   float* scale;   // [batch][H] (e4m3 copy)
   void* xbuf;     // [batch][H][cap][P]
   void* bbuf;     // [batch][G][cap][N]
   void* dtbuf;    // [batch][H][cap]
-  int4* meta;     // [batch] {start, n, pending, 0}
+  int4* meta;     // [batch] {start, n, pending, epoch of the next checkpoint write}
   int* arrive;    // [batch]
   int* status;
   int4* plan;     // [batch] {start, n, kind, 0} of the step in flight
@@ -40,6 +42,7 @@ struct StoreView {
   const float* A;
   const float* D;
   int batch, H, G, hpg, L, cap, tmax;
+  int shared;     // 1: the read copy is the checkpoint (no FP32 checkpoint)
 };
 
 // ------------------------------------------------------------------ element conversion
@@ -158,6 +161,54 @@ __device__ __forceinline__ void st_e4m3_stream(uint8_t* p, float scale, const fl
   }
 }
 
+// Read-copy "packs": the raw bytes of VEC consecutive copy elements, kept packed in registers
+// until they are used (so a thread can hold several heads' tiles), and their widening.
+template <int RC, int VEC> struct PackOf;
+template <> struct PackOf<REPLAY_RC_BF16, 4> { using type = uint2; };
+template <> struct PackOf<REPLAY_RC_BF16, 2> { using type = unsigned int; };
+template <> struct PackOf<REPLAY_RC_FP8E4M3, 4> { using type = unsigned int; };
+template <> struct PackOf<REPLAY_RC_FP8E4M3, 2> { using type = unsigned short; };
+template <> struct PackOf<REPLAY_RC_FP16, 4> { using type = uint2; };
+template <> struct PackOf<REPLAY_RC_FP16, 2> { using type = unsigned int; };
+
+template <int RC, int VEC>
+__device__ __forceinline__ typename PackOf<RC, VEC>::type ld_pack(const void* rc, size_t elem) {
+  using PT = typename PackOf<RC, VEC>::type;
+  constexpr int esz = RC == REPLAY_RC_FP8E4M3 ? 1 : 2;
+  return __ldcs(reinterpret_cast<const PT*>(static_cast<const char*>(rc) + elem * esz));
+}
+template <int RC, int VEC>
+__device__ __forceinline__ void unpack(typename PackOf<RC, VEC>::type v, float scale, float (&o)[VEC]) {
+  if constexpr (RC == REPLAY_RC_BF16) {
+    if constexpr (VEC == 4) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+      o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+    } else {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+      o[0] = a.x; o[1] = a.y;
+    }
+  } else if constexpr (RC == REPLAY_RC_FP16) {
+    if constexpr (VEC == 4) {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+      o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+    } else {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v));
+      o[0] = a.x; o[1] = a.y;
+    }
+  } else {
+    if constexpr (VEC == 4) {
+      const float2 a = e4m3x2_to_float2(static_cast<unsigned short>(v & 0xffffu));
+      const float2 b = e4m3x2_to_float2(static_cast<unsigned short>(v >> 16));
+      o[0] = a.x * scale; o[1] = a.y * scale; o[2] = b.x * scale; o[3] = b.y * scale;
+    } else {
+      const float2 a = e4m3x2_to_float2(v);
+      o[0] = a.x * scale; o[1] = a.y * scale;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ slab register tile
 // A P x N slab is spread over 8 warps: warp w owns rows w*RPW .. w*RPW+RPW-1; in each row a
 // lane owns NVEC vectors of VEC columns, vector v at column v*32*VEC + lane*VEC. Every
@@ -217,7 +268,58 @@ __device__ __forceinline__ void store_tile_f32(float* slab, int warp, int lane,
     }
 }
 
-// Read-copy tile loads/stores. RC is REPLAY_RC_BF16 or REPLAY_RC_FP8E4M3.
+// FP16 copies: loads, round-to-nearest-even stores, and stochastic rounding.
+template <int VEC>
+__device__ __forceinline__ void ld_f16_stream(const __half* p, float (&o)[VEC]) {
+  if constexpr (VEC == 4) {
+    uint2 v = __ldcs(reinterpret_cast<const uint2*>(p));
+    const float2 a = __half22float2(*reinterpret_cast<__half2*>(&v.x));
+    const float2 b = __half22float2(*reinterpret_cast<__half2*>(&v.y));
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+  } else {
+    unsigned int v = __ldcs(reinterpret_cast<const unsigned int*>(p));
+    const float2 a = __half22float2(*reinterpret_cast<__half2*>(&v));
+    o[0] = a.x; o[1] = a.y;
+  }
+}
+template <int VEC>
+__device__ __forceinline__ void st_f16_stream(__half* p, const float (&v)[VEC]) {
+  if constexpr (VEC == 4) {
+    __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<unsigned int*>(&a);
+    u.y = *reinterpret_cast<unsigned int*>(&b);
+    __stcs(reinterpret_cast<uint2*>(p), u);
+  } else {
+    __half2 a = __floats2half2_rn(v[0], v[1]);
+    __stcs(reinterpret_cast<unsigned int*>(p), *reinterpret_cast<unsigned int*>(&a));
+  }
+}
+
+// The draws of stochastic rounding: output idx of the splitmix64 sequence (Steele, Lea and
+// Flood, "Fast splittable pseudorandom number generators", OOPSLA 2014) started at kSrSeed;
+// its top 24 bits give u in [0, 1).
+constexpr unsigned long long kSrSeed = 0x2545F4914F6CDD1Dull;
+__device__ __forceinline__ unsigned long long splitmix64_at(unsigned long long seed, unsigned long long idx) {
+  unsigned long long z = seed + (idx + 1ull) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+// FP32 -> FP16 code by stochastic rounding: with lo the FP16 value toward zero and hi the
+// next one away from zero, take hi iff u < (|v| - |lo|) / (|hi| - |lo|). Both differences
+// are exact and the step is a power of two, so the ratio is exact. Saturates at 65504.
+__device__ __forceinline__ unsigned short f16_sr(float v, float u) {
+  const unsigned short lb = __half_as_ushort(__float2half_rz(v));
+  if ((lb & 0x7FFFu) >= 0x7BFFu) return static_cast<unsigned short>((lb & 0x8000u) | 0x7BFFu);
+  const unsigned short hb = static_cast<unsigned short>(lb + 1u);
+  const float lo = fabsf(__half2float(__ushort_as_half(lb)));
+  const float hi = fabsf(__half2float(__ushort_as_half(hb)));
+  const float frac = __fdiv_rn(fabsf(v) - lo, hi - lo);
+  return u < frac ? hb : lb;
+}
+
+// Read-copy tile loads/stores. RC is REPLAY_RC_BF16, REPLAY_RC_FP8E4M3 or REPLAY_RC_FP16.
 template <int P, int N, int RC>
 __device__ __forceinline__ void load_tile_rc(const void* rc, size_t slab, float scale, int warp,
                                              int lane, float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
@@ -230,6 +332,8 @@ __device__ __forceinline__ void load_tile_rc(const void* rc, size_t slab, float 
       const size_t off = slab * P * N + TL::row(warp, i) * N + TL::col(lane, v);
       if constexpr (RC == REPLAY_RC_BF16)
         ld_bf16_stream<TL::VEC>(static_cast<const bf16*>(rc) + off, t);
+      else if constexpr (RC == REPLAY_RC_FP16)
+        ld_f16_stream<TL::VEC>(static_cast<const __half*>(rc) + off, t);
       else
         ld_e4m3_stream<TL::VEC>(static_cast<const uint8_t*>(rc) + off, scale, t);
 #pragma unroll
@@ -251,8 +355,41 @@ __device__ __forceinline__ void store_tile_rc(void* rc, size_t slab, float scale
       const size_t off = slab * P * N + TL::row(warp, i) * N + TL::col(lane, v);
       if constexpr (RC == REPLAY_RC_BF16)
         st_bf16_stream<TL::VEC>(static_cast<bf16*>(rc) + off, t);
+      else if constexpr (RC == REPLAY_RC_FP16)
+        st_f16_stream<TL::VEC>(static_cast<__half*>(rc) + off, t);
       else
         st_e4m3_stream<TL::VEC>(static_cast<uint8_t*>(rc) + off, scale, t);
+    }
+}
+
+// An FP16 tile by stochastic rounding: element e of slab `slab` (of num_slabs) written by
+// flush `epoch` draws u from index (epoch * num_slabs + slab) * P*N + e.
+template <int P, int N>
+__device__ __forceinline__ void store_tile_f16_sr(void* rc, size_t slab, unsigned long long epoch,
+                                                  unsigned long long num_slabs, int warp, int lane,
+                                                  const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+  const unsigned long long base = (epoch * num_slabs + slab) * static_cast<unsigned long long>(P * N);
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+    for (int v = 0; v < TL::NVEC; ++v) {
+      const int e0 = TL::row(warp, i) * N + TL::col(lane, v);
+      unsigned short c[TL::VEC];
+#pragma unroll
+      for (int e = 0; e < TL::VEC; ++e) {
+        const float u = static_cast<float>(splitmix64_at(kSrSeed, base + e0 + e) >> 40) * 0x1p-24f;
+        c[e] = f16_sr(hv[i][v * TL::VEC + e], u);
+      }
+      __half* p = static_cast<__half*>(rc) + slab * P * N + e0;
+      if constexpr (TL::VEC == 4) {
+        uint2 w;
+        w.x = c[0] | (static_cast<unsigned int>(c[1]) << 16);
+        w.y = c[2] | (static_cast<unsigned int>(c[3]) << 16);
+        __stcs(reinterpret_cast<uint2*>(p), w);
+      } else {
+        __stcs(reinterpret_cast<unsigned int*>(p), c[0] | (static_cast<unsigned int>(c[1]) << 16));
+      }
     }
 }
 

@@ -15,14 +15,17 @@ struct Shape {
   int P, N, in_dtype, read_copy;
 };
 
-// Every (dstate, input type, read copy) combination with a kernel; headdim is 64.
+// Every (dstate, input type, read copy) combination with a kernel; headdim is 64. The FP16
+// copy has kernels for dstate 64 and 128.
 #define RSSM_FOR_EACH_CONFIG(X)                                                    \
   X(128, float, REPLAY_RC_NONE) X(128, float, REPLAY_RC_BF16) X(128, float, REPLAY_RC_FP8E4M3) \
   X(128, bf16, REPLAY_RC_NONE) X(128, bf16, REPLAY_RC_BF16) X(128, bf16, REPLAY_RC_FP8E4M3)   \
   X(64, float, REPLAY_RC_NONE) X(64, float, REPLAY_RC_BF16) X(64, float, REPLAY_RC_FP8E4M3)    \
   X(64, bf16, REPLAY_RC_NONE) X(64, bf16, REPLAY_RC_BF16) X(64, bf16, REPLAY_RC_FP8E4M3)      \
   X(256, float, REPLAY_RC_NONE) X(256, float, REPLAY_RC_BF16) X(256, float, REPLAY_RC_FP8E4M3) \
-  X(256, bf16, REPLAY_RC_NONE) X(256, bf16, REPLAY_RC_BF16) X(256, bf16, REPLAY_RC_FP8E4M3)
+  X(256, bf16, REPLAY_RC_NONE) X(256, bf16, REPLAY_RC_BF16) X(256, bf16, REPLAY_RC_FP8E4M3)   \
+  X(128, float, REPLAY_RC_FP16) X(128, bf16, REPLAY_RC_FP16) X(64, float, REPLAY_RC_FP16)      \
+  X(64, bf16, REPLAY_RC_FP16)
 
 #define RSSM_DTYPE_OF(TT) (std::is_same<TT, float>::value ? REPLAY_F32 : REPLAY_BF16)
 

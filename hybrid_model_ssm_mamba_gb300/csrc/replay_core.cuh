@@ -111,16 +111,26 @@ __device__ __forceinline__ void append_record(const SlabRing<T>& ring, const Rin
 
 // Write a new checkpoint tile: FP32 always, and the read copy cast independently from the
 // same FP32 values ("Benefit 3: Limit error accumulation with separate precisions"). The
-// E4M3 copy takes one FP32 scale per slab, absmax / 448 (1 for an all-zero slab). Contains
-// CTA barriers when the copy is E4M3.
+// E4M3 copy takes one FP32 scale per slab, absmax / 448 (1 for an all-zero slab). An FP16
+// copy rounds to nearest even, except when it is itself the checkpoint: then it is rounded
+// stochastically, with draws indexed by the sequence's flush count `epoch` (the FP16
+// recurrence checkpoint with stochastic rounding the post's section "State quantization"
+// cites). Contains CTA barriers when the copy is E4M3.
 template <int P, int N, int RC>
 __device__ __forceinline__ void write_checkpoint(const StoreView& sv, size_t slab, float* s_red,
-                                                 const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+                                                 const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E],
+                                                 int epoch) {
   using TL = Tile<P, N>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  store_tile_f32<P, N>(sv.h0 + slab * P * N, warp, lane, hv);
+  if (!sv.shared) store_tile_f32<P, N>(sv.h0 + slab * P * N, warp, lane, hv);  // shared: copy only
   if constexpr (RC == REPLAY_RC_BF16) {
     store_tile_rc<P, N, RC>(sv.rc, slab, 1.f, warp, lane, hv);
+  } else if constexpr (RC == REPLAY_RC_FP16) {
+    if (sv.shared)
+      store_tile_f16_sr<P, N>(sv.rc, slab, static_cast<unsigned int>(epoch),
+                              static_cast<unsigned long long>(sv.batch) * sv.H, warp, lane, hv);
+    else
+      store_tile_rc<P, N, RC>(sv.rc, slab, 1.f, warp, lane, hv);
   } else if constexpr (RC == REPLAY_RC_FP8E4M3) {
     float m = 0.f;
 #pragma unroll

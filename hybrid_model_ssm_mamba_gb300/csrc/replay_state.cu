@@ -28,7 +28,12 @@ replay_fold_kernel(StoreView sv, float* __restrict__ out) {
 
   if (tid == 0) s_meta = sv.meta[b];
   float hv[TL::RPW][TL::E];
-  load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+  if (RC != REPLAY_RC_NONE && sv.shared) {  // the copy is the checkpoint
+    const float scale = RC == REPLAY_RC_FP8E4M3 ? sv.scale[slab] : 1.f;
+    load_tile_rc<P, N, RC == REPLAY_RC_NONE ? REPLAY_RC_BF16 : RC>(sv.rc, slab, scale, warp, lane, hv);
+  } else {
+    load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+  }
   __syncthreads();
   const int start = s_meta.x, n = s_meta.y;
   if (n < 0 || n > cap || start < 0 || start >= cap) {
@@ -47,7 +52,7 @@ replay_fold_kernel(StoreView sv, float* __restrict__ out) {
   const ExtraRecords<T> none{nullptr, nullptr, nullptr, 0, 0, 0};
   stage_records<P, N, T>(ring, im, start, cap, n, n, none);
   if constexpr (MODE == 0) {
-    if (tid == 0) arrive_and_publish(sv, b, make_int4(ring_slot(start, n, cap), 0, 0, 0), sv.H);
+    if (tid == 0) arrive_and_publish(sv, b, make_int4(ring_slot(start, n, cap), 0, 0, s_meta.w + (n > 0)), sv.H);
   }
   cp_async_wait_all();
   __syncthreads();
@@ -59,7 +64,7 @@ replay_fold_kernel(StoreView sv, float* __restrict__ out) {
   if constexpr (MODE == 1) {
     store_tile_f32<P, N>(out + static_cast<size_t>(slab) * P * N, warp, lane, hv);
   } else {
-    if (n > 0) write_checkpoint<P, N, RC>(sv, slab, s_red, hv);
+    if (n > 0) write_checkpoint<P, N, RC>(sv, slab, s_red, hv, s_meta.w);
   }
 }
 
@@ -82,9 +87,9 @@ replay_load_kernel(StoreView sv, const float* __restrict__ h, const int* __restr
 #pragma unroll
       for (int e = 0; e < TL::E; ++e) hv[i][e] = 0.f;
   }
-  write_checkpoint<P, N, RC>(sv, slab, s_red, hv);
+  write_checkpoint<P, N, RC>(sv, slab, s_red, hv, 0);
   if (hd == 0 && tid == 0) {
-    sv.meta[b] = make_int4(0, 0, 0, 0);
+    sv.meta[b] = make_int4(0, 0, 0, 1);
     sv.arrive[b] = 0;
   }
 }
@@ -121,6 +126,7 @@ int launch_load(const StoreView& sv, const Shape& sh, const float* h, const int*
   RSSM_LOAD(64, REPLAY_RC_NONE) RSSM_LOAD(64, REPLAY_RC_BF16) RSSM_LOAD(64, REPLAY_RC_FP8E4M3)
   RSSM_LOAD(128, REPLAY_RC_NONE) RSSM_LOAD(128, REPLAY_RC_BF16) RSSM_LOAD(128, REPLAY_RC_FP8E4M3)
   RSSM_LOAD(256, REPLAY_RC_NONE) RSSM_LOAD(256, REPLAY_RC_BF16) RSSM_LOAD(256, REPLAY_RC_FP8E4M3)
+  RSSM_LOAD(64, REPLAY_RC_FP16) RSSM_LOAD(128, REPLAY_RC_FP16)
 #undef RSSM_LOAD
   return REPLAY_EUNSUPPORTED;
 }

@@ -29,13 +29,16 @@ namespace rssm {
 constexpr int kMaxDrafts = 8;
 constexpr int kVerifyBad = -1, kVerifyPlain = 0, kVerifyPrefold = 1;
 
+constexpr int kPrepThreads = 128, kPrepWarps = kPrepThreads / 32;  // small: see the step's prep
+
 template <int P, int N, class T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kPrepThreads)
 replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T* __restrict__ C,
                           const T* __restrict__ dt) {
   using TL = Tile<P, N>;
   __shared__ int4 s_meta;
   __shared__ float s_bc[kMaxDrafts][kMaxCap];
+  __shared__ float s_dt[kDtStage];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x, b = blockIdx.y;
   const int H = sv.H, G = sv.G, cap = sv.cap;
@@ -43,10 +46,10 @@ replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T
   griddep_launch_dependents();  // the head CTAs may start their checkpoint loads now
   if (tid == 0) s_meta = sv.meta[b];
   __syncthreads();
-  const int start = s_meta.x, n = s_meta.y;
+  const int start = s_meta.x, n = s_meta.y, epoch = s_meta.w;
   if (n < 0 || start < 0 || start >= cap || n + TT > cap) {
     if (tid == 0) {
-      if (g == 0) sv.plan[b] = make_int4(start, n, kVerifyBad, 0);
+      if (g == 0) sv.plan[b] = make_int4(start, n, kVerifyBad, epoch);
       set_status(sv.status, REPLAY_DEV_BAD_META);
     }
     return;
@@ -55,26 +58,41 @@ replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T
   const int start2 = prefold ? ring_slot(start, n, cap) : start;
   const int n2 = prefold ? 0 : n;
   if (tid == 0) {
-    if (g == 0) sv.plan[b] = make_int4(start, n, prefold ? kVerifyPrefold : kVerifyPlain, 0);
-    arrive_and_publish(sv, b, make_int4(start2, n2, TT, 0), G);
+    if (g == 0) sv.plan[b] = make_int4(start, n, prefold ? kVerifyPrefold : kVerifyPlain, epoch);
+    arrive_and_publish(sv, b, make_int4(start2, n2, TT, epoch + (prefold ? 1 : 0)), G);
   }
   const T* bring = static_cast<const T*>(sv.bbuf) + (static_cast<size_t>(b) * G + g) * cap * N;
   const int kk = n2 + TT;  // committed records after any pre-fold, then the drafts
-  // stage the kk records' B and the TT queries' C in shared memory (one round trip)
+  // every head's dt values -- the pre-folded records', then the queries' records' -- in one
+  // round trip (when they fit), beside the B and C staging below
+  const int nf = prefold ? n : 0, per = nf + kk;
+  const bool stage_dt = sv.hpg * per <= kDtStage;
+  auto dt_rec = [&](int hh, int i) {
+    const size_t slab = static_cast<size_t>(b) * H + g * sv.hpg + hh;
+    const T* dtr = static_cast<const T*>(sv.dtbuf) + slab * cap;
+    if (i < nf) return to_f(dtr[ring_slot(start, i, cap)]);
+    const int s = i - nf;
+    return to_f(s < n2 ? dtr[ring_slot(start2, s, cap)]
+                       : dt[(static_cast<size_t>(b) * TT + (s - n2)) * H + g * sv.hpg + hh]);
+  };
+  // stage the kk records' B and the TT queries' C in shared memory by cp.async, and the dt
+  // values meanwhile: one round trip
   extern __shared__ float4 smem4[];
   T* sb = reinterpret_cast<T*>(smem4);  // [kk][N] B of the records, then [TT][N] C of the drafts
   {
     constexpr int EPC = 16 / sizeof(T), BC = N / EPC;
-    for (int c = tid; c < (kk + TT) * BC; c += kThreads) {
+    for (int c = tid; c < (kk + TT) * BC; c += kPrepThreads) {
       const int r = c / BC, off = (c - r * BC) * EPC;
       const T* src = r >= kk ? C + boff(r - kk)
                              : (r < n2 ? bring + static_cast<size_t>(ring_slot(start2, r, cap)) * N : B + boff(r - n2));
       cp_async16(sb + static_cast<size_t>(r) * N + off, src + off);
     }
+    if (stage_dt)
+      for (int idx = tid; idx < sv.hpg * per; idx += kPrepThreads) s_dt[idx] = dt_rec(idx / per, idx % per);
     cp_async_wait_all();
     __syncthreads();
   }
-  for (int pi = warp; pi < TT * kk; pi += kWarps) {
+  for (int pi = warp; pi < TT * kk; pi += kPrepWarps) {
     const int j = pi / kk, s = pi - j * kk;
     if (s > n2 + j) continue;
     float bv[TL::E], cj[TL::E];
@@ -88,19 +106,17 @@ replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T
   }
   __syncthreads();
   const int cs = cap + 1;
-  for (int hh = warp; hh < sv.hpg; hh += kWarps) {
+  for (int hh = warp; hh < sv.hpg; hh += kPrepWarps) {
     const int h = g * sv.hpg + hh;
     const size_t slab = static_cast<size_t>(b) * H + h;
     const float A = sv.A[h];
-    const T* dtr = static_cast<const T*>(sv.dtbuf) + slab * cap;
     float* cf = sv.coef + slab * (sv.tmax + 1) * cs;
+    auto dt_at = [&](int i) { return stage_dt ? s_dt[hh * per + i] : dt_rec(hh, i); };
     if (prefold) {
-      auto dt_fold = [&](int s) { return to_f(dtr[ring_slot(start, s, cap)]); };
+      auto dt_fold = [&](int s) { return dt_at(s); };
       write_fold_weights(dt_fold, n, A, cf, cap, lane);
     }
-    auto dt_q = [&](int s) {
-      return to_f(s < n2 ? dtr[ring_slot(start2, s, cap)] : dt[(static_cast<size_t>(b) * TT + (s - n2)) * H + h]);
-    };
+    auto dt_q = [&](int s) { return dt_at(nf + s); };
     const float d0 = lane < kk ? dt_q(lane) : 0.f;
     const float d1 = lane + 32 < kk ? dt_q(lane + 32) : 0.f;
     for (int j = 0; j < TT; ++j) {
@@ -174,8 +190,9 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
   const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
 
   if (prefold) {  // a flush of the committed records, from the FP32 checkpoint
-    if constexpr (RC != REPLAY_RC_NONE)
-      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    if constexpr (RC != REPLAY_RC_NONE) {
+      if (!sv.shared) load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    }
     float* sm_u = reinterpret_cast<float*>(smem4);
     float* sm_b = sm_u + cap * P;
     auto xf = [&](int s) { return ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P; };
@@ -183,7 +200,7 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
     stage_weighted<P, N, T>(xf, bf, cf, n, sm_u, sm_b);
     __syncthreads();
     fold_staged<P, N>(sm_u, sm_b, n, cf[cap], hv);
-    write_checkpoint<P, N, RC>(sv, slab, s_red, hv);
+    write_checkpoint<P, N, RC>(sv, slab, s_red, hv, pl.w);
   }
 
   const int kk = n2 + TT;
@@ -233,7 +250,7 @@ static int launch(const StoreView& sv, int TT, const void* x, const void* B, con
       cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
-  prep<<<dim3(sv.G, sv.batch), kThreads, psmem, stream>>>(sv, TT, static_cast<const T*>(B),
+  prep<<<dim3(sv.G, sv.batch), kPrepThreads, psmem, stream>>>(sv, TT, static_cast<const T*>(B),
                                                           static_cast<const T*>(C), static_cast<const T*>(dt));
   if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
   auto kern = replay_verify_kernel<P, N, T, RC>;

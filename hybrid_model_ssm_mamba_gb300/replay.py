@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = [
     "ReplayError", "ReplayConfig", "ReplayLayout", "load_library", "header_functions",
-    "REPLAY_F32", "REPLAY_BF16", "REPLAY_RC_NONE", "REPLAY_RC_BF16", "REPLAY_RC_FP8E4M3",
+    "REPLAY_F32", "REPLAY_BF16", "REPLAY_RC_NONE", "REPLAY_RC_BF16", "REPLAY_RC_FP8E4M3", "REPLAY_RC_FP16",
     "REPLAY_DEV_BAD_META", "REPLAY_DEV_BAD_ACCEPT",
     "replay_layout_of", "replay_store_bytes", "replay_alloc", "replay_free", "replay_reset",
     "replay_load_state", "replay_export_state", "replay_step", "replay_verify",
@@ -30,7 +30,7 @@ __all__ = [
 HEADER = pathlib.Path(__file__).resolve().parent.parent / "include" / "replayssm.h"
 
 REPLAY_F32, REPLAY_BF16 = 0, 1
-REPLAY_RC_NONE, REPLAY_RC_BF16, REPLAY_RC_FP8E4M3 = 0, 1, 2
+REPLAY_RC_NONE, REPLAY_RC_BF16, REPLAY_RC_FP8E4M3, REPLAY_RC_FP16 = 0, 1, 2, 3
 REPLAY_DEV_BAD_META, REPLAY_DEV_BAD_ACCEPT = 1, 2
 REPLAY_STATIC_MAX_BATCH = 4096
 REPLAY_STATIC_MAX_COEFS = 1048576
@@ -47,12 +47,12 @@ class ReplayError(RuntimeError):
 class ReplayConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "batch", "nheads", "headdim", "dstate", "ngroups", "window_L", "max_draft_T",
-        "in_dtype", "read_copy")]
+        "in_dtype", "read_copy", "shared_checkpoint")]
 
     def __init__(self, batch, nheads, headdim, dstate, ngroups, window_L=16, max_draft_T=0,
-                 in_dtype=REPLAY_F32, read_copy=REPLAY_RC_NONE):
+                 in_dtype=REPLAY_F32, read_copy=REPLAY_RC_NONE, shared_checkpoint=0):
         super().__init__(batch, nheads, headdim, dstate, ngroups, window_L, max_draft_T,
-                         in_dtype, read_copy)
+                         in_dtype, read_copy, shared_checkpoint)
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -289,8 +289,9 @@ class ReplayStore:
         Bz, H, P, N, G, cap = c.batch, c.nheads, c.headdim, c.dstate, c.ngroups, L.cap
         dt = self.in_dtype
         spec = {
-            "h0": (torch.float32, (Bz, H, P, N)),
-            "rc": ({REPLAY_RC_BF16: torch.bfloat16, REPLAY_RC_FP8E4M3: torch.uint8}.get(c.read_copy, torch.uint8),
+            "h0": (torch.float32, (0,) if c.shared_checkpoint else (Bz, H, P, N)),
+            "rc": ({REPLAY_RC_BF16: torch.bfloat16, REPLAY_RC_FP8E4M3: torch.uint8,
+                    REPLAY_RC_FP16: torch.float16}.get(c.read_copy, torch.uint8),
                    (Bz, H, P, N) if c.read_copy else (0,)),
             "scale": (torch.float32, (Bz, H) if c.read_copy == REPLAY_RC_FP8E4M3 else (0,)),
             "xbuf": (dt, (Bz, H, cap, P)), "bbuf": (dt, (Bz, G, cap, N)), "dtbuf": (dt, (Bz, H, cap)),

@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define REPLAY_ABI_VERSION 1
+#define REPLAY_ABI_VERSION 2
 
 /* element types of x, B, C, dt and of the ring records */
 #define REPLAY_F32 0
@@ -56,6 +56,17 @@ extern "C" {
 #define REPLAY_RC_NONE 0
 #define REPLAY_RC_BF16 1     /* bf16, round to nearest even */
 #define REPLAY_RC_FP8E4M3 2  /* OCP E4M3, RNE, saturating; FP32 scale absmax/448 per (b, h) */
+#define REPLAY_RC_FP16 3     /* IEEE binary16. As a separate copy: round to nearest even. As the
+                              * shared checkpoint (shared_checkpoint = 1): stochastic rounding,
+                              * saturating at +-65504 -- the FP16 recurrence checkpoint with
+                              * stochastic rounding named in the post's section "State
+                              * quantization". The draw for element e (row-major in P x N) of
+                              * slab s = b*H + h, written by the sequence's flush number `epoch`
+                              * (meta.w), is output (epoch*batch*H + s)*P*N + e of the splitmix64
+                              * generator seeded 0x2545F4914F6CDD1D; its top 24 bits over 2^24
+                              * give u, and the value rounds away from zero iff u is below its
+                              * distance from the lower neighbour over the neighbours' spacing.
+                              * dstate 64 and 128 only. */
 
 /* host return codes */
 #define REPLAY_OK 0
@@ -78,17 +89,24 @@ typedef struct replay_config {
   int max_draft_T;  /* largest T passed to replay_verify; 0 = no speculative verify */
   int in_dtype;     /* REPLAY_F32 or REPLAY_BF16 */
   int read_copy;    /* REPLAY_RC_* */
+  int shared_checkpoint; /* 0: FP32 checkpoint + derived read copy ("Benefit 3", separate
+                          * precisions). 1: the low-precision copy IS the checkpoint: flushes
+                          * start from it and write only it, no FP32 checkpoint is kept (the
+                          * "shared" low-precision checkpoint the pages compare against: rounded
+                          * once per window, and fed back). Needs read_copy != REPLAY_RC_NONE. */
 } replay_config;
 
 /* Byte offsets of the regions inside the caller's workspace (each 256-byte aligned).
  *   h0     FP32 checkpoint            [batch][H][P][N]
- *   rc     read copy (bf16 or E4M3)   [batch][H][P][N]      (0 bytes without a copy)
+ *   rc     read copy (bf16/E4M3/FP16) [batch][H][P][N]      (0 bytes without a copy)
  *   scale  FP32 E4M3 scale            [batch][H]            (0 bytes unless E4M3)
  *   xbuf   ring of x records          [batch][H][cap][P]    (in_dtype)
  *   bbuf   ring of B records          [batch][G][cap][N]    (in_dtype)
  *   dtbuf  ring of dt records         [batch][H][cap]       (in_dtype)
- *   meta   per sequence int32 x4      {start, n, pending, 0}: records live in ring slots
- *          (start + s) mod cap, s < n; `pending` drafts sit beyond them after a verify
+ *   meta   per sequence int32 x4      {start, n, pending, epoch}: records live in ring slots
+ *          (start + s) mod cap, s < n; `pending` drafts sit beyond them after a verify;
+ *          `epoch` numbers the sequence's next checkpoint write (the load/reset write is
+ *          number 0, so it is 1 after a load and grows by one at each flush)
  *   arrive per sequence int32 counter (internal; zero between calls)
  *   status int32 device status word (REPLAY_DEV_* bits)
  *   plan   per sequence int32 x4      (internal, per step: the pointer the step runs on)

@@ -19,6 +19,17 @@ rounding nor the scale; the readings taken here are:
   is all zero); codes ``q = e4m3(h / scale)``; the value read back is ``decode(q) * scale``.
   Both divisions are single IEEE binary32 divisions, so the code of each element is
   decided in FP32.
+* NVFP4 (the post's sections "Benefit 3" and "State quantization" name it; the format is
+  NVIDIA's published 4-bit block format): E2M1 elements (1 sign, 2 exponent bits with
+  bias 1, 1 fraction bit; exponent field 0 holds 0 and 0.5; largest value 6; no inf or
+  NaN), one E4M3 scale per block of 16 consecutive elements of a row, and one FP32 scale
+  per tensor -- here per (sequence, head) slab, like the E4M3 copy. The scales follow the
+  usual two-level recipe, each step one FP32 operation:
+  ``s_g = absmax / (448 * 6)`` (``1`` for an all-zero slab); for each block
+  ``s_b = e4m3(block_absmax / (6 * s_g))``; ``e = decode(s_b) * s_g``; codes
+  ``q = e2m1(h / e)`` (round to nearest, ties to even, saturating at +-6), or 0 for the
+  whole block when ``e`` is 0; the value read back is ``decode(q) * e``. Two codes share a
+  byte, the even element in the low nibble.
 """
 from __future__ import annotations
 
@@ -27,6 +38,8 @@ import numpy as np
 __all__ = [
     "bf16_encode", "bf16_decode", "e4m3_decode", "e4m3_encode",
     "E4M3_MAX", "fp8_slab_quantize", "fp8_slab_dequantize",
+    "E2M1_MAX", "NVFP4_BLOCK", "e2m1_decode", "e2m1_encode", "nvfp4_slab_quantize",
+    "nvfp4_slab_dequantize", "nvfp4_pack", "nvfp4_unpack", "nvfp4_round_state",
 ]
 
 E4M3_MAX = 448.0
@@ -116,3 +129,191 @@ def fp8_slab_quantize(h) -> tuple[np.ndarray, np.float32]:
 def fp8_slab_dequantize(codes, scale) -> np.ndarray:
     """Value read back from a slab's codes: decode(q) * scale, in FP32."""
     return (e4m3_decode(codes).astype(np.float32) * np.float32(scale)).astype(np.float32)
+
+
+def bf16_round_state(h) -> np.ndarray:
+    """A state rounded to bf16 element by element (FP64 -> FP32 -> bf16 RNE), widened back."""
+    return bf16_decode(bf16_encode(np.asarray(h, dtype=np.float64).astype(np.float32))).astype(np.float64)
+
+
+def e4m3_round_state(h) -> np.ndarray:
+    """A state [..., P, N] rounded to E4M3 with one absmax scale per P x N slab, widened back."""
+    h32 = np.asarray(h, dtype=np.float64).astype(np.float32)
+    out = np.empty(h32.shape, dtype=np.float64)
+    lead = h32.shape[:-2]
+    for idx in np.ndindex(*lead):
+        q, s = fp8_slab_quantize(h32[idx])
+        out[idx] = fp8_slab_dequantize(q, s)
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# IEEE binary16 (FP16): 1 sign, 5 exponent (bias 15), 10 fraction bits; exponent field 0
+# holds subnormals m * 2**-24; largest finite value 65504.
+
+def fp16_decode(bits) -> np.ndarray:
+    """FP16 bit patterns -> FP64 values."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    s = np.where(b & 0x8000, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    m = (b & 0x3FF).astype(np.float64)
+    v = np.where(e == 0, m * 2.0 ** -24, (1.0 + m / 1024.0) * np.exp2(e.astype(np.float64) - 15.0))
+    v = np.where(e == 31, np.where(m == 0, np.inf, np.nan), v)
+    return s * v
+
+
+_F16_POS = fp16_decode(np.arange(0x7C00, dtype=np.uint16))   # finite non-negative, ascending
+FP16_MAX = 65504.0
+
+
+def fp16_neighbours(v):
+    """For FP32 values v: the FP16 code toward zero (lo) and the code next away from zero
+    (hi), as bit patterns with v's sign, and their magnitudes. Past 65504 both are 65504."""
+    f = np.asarray(v, dtype=np.float32).astype(np.float64)
+    a = np.abs(f)
+    i = np.searchsorted(_F16_POS, a, side="right") - 1          # largest code <= |v|
+    i = np.clip(i, 0, len(_F16_POS) - 1)
+    j = np.minimum(i + 1, len(_F16_POS) - 1)
+    sign = np.where(np.signbit(f), 0x8000, 0)
+    return ((i | sign).astype(np.uint16), (j | sign).astype(np.uint16), _F16_POS[i], _F16_POS[j])
+
+
+def fp16_encode(v) -> np.ndarray:
+    """FP32 -> FP16 codes, round to nearest, ties to even; finite values past the largest
+    step round to infinity (IEEE)."""
+    lo, hi, lv, hv = fp16_neighbours(v)
+    a = np.abs(np.asarray(v, dtype=np.float32).astype(np.float64))
+    top = (lo & 0x7FFF) == 0x7BFF
+    hv = np.where(top, 65536.0, hv)                              # the next step past 65504
+    d_lo, d_hi = a - lv, hv - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((lo & 1) == 1))
+    out = np.where(pick_hi, np.where(top, (lo & 0x8000) | 0x7C00, hi), lo)
+    return out.astype(np.uint16)
+
+
+def fp16_sr_encode(v, u) -> np.ndarray:
+    """FP32 -> FP16 codes by stochastic rounding: with lo and hi the FP16 neighbours of v
+    (toward zero / away from zero), round to hi iff u < (|v| - |lo|) / (|hi| - |lo|), u in
+    [0, 1). The ratio is exact in FP32 (the step is a power of two), so the decision is the
+    same in any precision. Values past 65504 saturate to +-65504."""
+    lo, hi, lv, hv = fp16_neighbours(v)
+    a = np.abs(np.asarray(v, dtype=np.float32).astype(np.float64))
+    with np.errstate(invalid="ignore", divide="ignore"):
+        frac = np.where(hv > lv, (a - lv) / (hv - lv), 0.0)
+    return np.where(np.asarray(u, dtype=np.float64) < frac, hi, lo).astype(np.uint16)
+
+
+# The random draws of stochastic rounding: value idx of the splitmix64 sequence (Steele,
+# Lea and Flood, OOPSLA 2014) started at SR_SEED, reduced to its top 24 bits: u = z >> 40,
+# u / 2**24 in [0, 1). For the checkpoint of slab `slab` (of `num_slabs`) written by flush
+# number `epoch`, element `elem` of P*N uses idx = (epoch * num_slabs + slab) * (P*N) + elem.
+SR_SEED = 0x2545F4914F6CDD1D
+_SM_GAMMA, _SM_M1, _SM_M2 = 0x9E3779B97F4A7C15, 0xBF58476D1CE4E5B9, 0x94D049BB133111EB
+
+
+def splitmix64(seed: int, idx) -> np.ndarray:
+    """Output idx (0-based) of the splitmix64 sequence whose state starts at seed."""
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed) + (np.asarray(idx, dtype=np.uint64) + np.uint64(1)) * np.uint64(_SM_GAMMA)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(_SM_M1)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(_SM_M2)
+        return z ^ (z >> np.uint64(31))
+
+
+def sr_uniform(idx) -> np.ndarray:
+    """u in [0, 1) (multiples of 2**-24) for draw indices idx (uint64)."""
+    return (splitmix64(SR_SEED, idx) >> np.uint64(40)).astype(np.float64) * 2.0 ** -24
+
+
+def fp16_sr_round_state(h, epoch: int, slabs, num_slabs: int) -> np.ndarray:
+    """A state [b, H, P, N] rounded to FP16 by stochastic rounding, widened back: slab
+    (b, h) has index slabs[b] * H + h among num_slabs (so a subset of sequences can be
+    followed), and its draws are those of flush `epoch`."""
+    h32 = np.asarray(h, dtype=np.float64).astype(np.float32)
+    bsz, H, P, N = h32.shape
+    slab = (np.asarray(slabs, dtype=np.uint64).reshape(-1, 1) * np.uint64(H) +
+            np.arange(H, dtype=np.uint64).reshape(1, -1)).reshape(bsz, H, 1, 1)
+    elem = np.arange(P * N, dtype=np.uint64).reshape(1, 1, P, N)
+    idx = (np.uint64(epoch) * np.uint64(num_slabs) + slab) * np.uint64(P * N) + elem
+    return fp16_decode(fp16_sr_encode(h32, sr_uniform(idx)))
+
+
+# ---------------------------------------------------------------------------------------
+# NVFP4: E2M1 codes with a two-level scale (readings in the module docstring).
+E2M1_MAX = 6.0
+NVFP4_BLOCK = 16
+_E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])   # codes 0..7 by definition
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """E2M1 codes (low 4 bits) -> FP64 values: sign bit 3, exponent bits 2..1 (bias 1),
+    fraction bit 0; exponent 0 is subnormal (fraction * 0.5)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64) & 0xF
+    e = (c >> 1) & 0x3
+    m = (c & 0x1).astype(np.float64)
+    mag = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(e.astype(np.float64) - 1.0))
+    return np.where(c & 0x8, -mag, mag)
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """FP32 -> E2M1 codes: round to nearest, ties to even (fraction bit 0), saturate to
+    +-6. The sign bit is kept, zero included."""
+    f = np.asarray(v, dtype=np.float32).astype(np.float64)
+    a = np.abs(f)
+    i = np.clip(np.searchsorted(_E2M1_POS, a, side="left"), 1, len(_E2M1_POS) - 1)
+    lo, hi = _E2M1_POS[i - 1], _E2M1_POS[i]
+    d_lo, d_hi = a - lo, hi - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (((i - 1) & 1) == 1))
+    code = np.where(pick_hi, i, i - 1)
+    code = np.where(a >= E2M1_MAX, 7, code)
+    return (code | np.where(np.signbit(f), 0x8, 0)).astype(np.uint8)
+
+
+def nvfp4_slab_quantize(h):
+    """One FP32 slab [P, N] -> (E2M1 codes [P, N], E4M3 block-scale codes [P, N/16],
+    FP32 slab scale). Every step is the single FP32 operation the recipe states."""
+    h = np.asarray(h, dtype=np.float32)
+    P, N = h.shape
+    absmax = np.float32(np.max(np.abs(h))) if h.size else np.float32(0)
+    s_g = np.float32(1.0) if absmax == 0 else np.float32(absmax / np.float32(E4M3_MAX * E2M1_MAX))
+    blocks = h.reshape(P, N // NVFP4_BLOCK, NVFP4_BLOCK)
+    bmax = np.max(np.abs(blocks), axis=2).astype(np.float32)
+    s_b = e4m3_encode((bmax / (np.float32(E2M1_MAX) * s_g)).astype(np.float32))
+    e = (e4m3_decode(s_b).astype(np.float32) * s_g).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (blocks / e[:, :, None]).astype(np.float32)
+    q = np.where(e[:, :, None] > 0, e2m1_encode(r), 0).astype(np.uint8)
+    return q.reshape(P, N), s_b, s_g
+
+
+def nvfp4_slab_dequantize(q, s_b, s_g) -> np.ndarray:
+    """Value read back: decode(q) * (decode(s_b) * s_g), with the block scale product in
+    FP32 as in the recipe (the element product is exact in FP64)."""
+    q = np.asarray(q, dtype=np.uint8)
+    P, N = q.shape
+    e = (e4m3_decode(s_b).astype(np.float32) * np.float32(s_g)).astype(np.float64)
+    return (e2m1_decode(q).reshape(P, N // NVFP4_BLOCK, NVFP4_BLOCK) * e[:, :, None]).reshape(P, N)
+
+
+def nvfp4_pack(q) -> np.ndarray:
+    """Codes [..., N] -> bytes [..., N/2]: element 2j in the low nibble, 2j+1 in the high."""
+    q = np.asarray(q, dtype=np.uint8)
+    return (q[..., 0::2] & 0xF) | ((q[..., 1::2] & 0xF) << 4)
+
+
+def nvfp4_unpack(b) -> np.ndarray:
+    """Bytes [..., N/2] -> codes [..., N]."""
+    b = np.asarray(b, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = b & 0xF
+    out[..., 1::2] = b >> 4
+    return out
+
+
+def nvfp4_round_state(h) -> np.ndarray:
+    """A state [..., P, N] quantized slab by slab to NVFP4 and read back (FP64)."""
+    h32 = np.asarray(h, dtype=np.float64).astype(np.float32)
+    out = np.empty(h32.shape, dtype=np.float64)
+    for idx in np.ndindex(*h32.shape[:-2]):
+        out[idx] = nvfp4_slab_dequantize(*nvfp4_slab_quantize(h32[idx]))
+    return out

@@ -73,14 +73,23 @@ class Mamba2Decoder:
     and speed up verification" -- outputs are those of decoding the accepted prefix.
     """
 
-    def __init__(self, A, D, ngroups: int, h0):
+    def __init__(self, A, D, ngroups: int, h0, window_round=None, window_L=None):
+        """``window_round`` (optional, with ``window_L``): a low-precision checkpoint that is
+        also the recurrence state. After every ``window_L``-th decode step the state is
+        replaced by ``window_round(state)`` -- the periodic checkpoint of the blog post's
+        section "Benefit 3" (rounded once every L steps, and fed back); the output of that
+        step is read before the rounding."""
         self.A = np.asarray(A, dtype=np.float64)
         self.D = np.asarray(D, dtype=np.float64)
         self.ngroups = ngroups
         self.h = np.array(h0, dtype=np.float64, copy=True)
+        self.window_round, self.window_L, self.t = window_round, window_L, 0
 
     def step(self, x, B, C, dt):
         self.h, y = decode_step(self.h, x, B, C, dt, self.A, self.D)
+        self.t += 1
+        if self.window_round is not None and self.t % self.window_L == 0:
+            self.h = self.window_round(self.h)
         return y
 
     def verify(self, xs, Bs, Cs, dts):

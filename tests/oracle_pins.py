@@ -206,3 +206,32 @@ ALL_PINS = [
     pin_zero_input_pure_decay, pin_zero_state_single_update, pin_window_closed_form,
     pin_window_length_invariance, pin_draft_matrix_form, pin_verify_then_truncate,
 ]
+
+
+def pin_window_rounding_only_at_window_ends():
+    """The periodic low-precision checkpoint: with an identity rounding the decoder is the
+    plain one; a rounding is applied exactly once per window, after the window's last step,
+    and that step's output is read before it."""
+    xs, Bs, Cs, dts, A, D, h0 = _tiny_inputs(30, bsz=2, k=10, H=2, G=1, P=2, N=3)
+    calls = []
+
+    def count(h):
+        calls.append(1)
+        return h
+
+    plain = m2.Mamba2Decoder(A, D, 1, h0)
+    counted = m2.Mamba2Decoder(A, D, 1, h0, window_round=count, window_L=4)
+    zeroing = m2.Mamba2Decoder(A, D, 1, h0, window_round=np.zeros_like, window_L=4)
+    for t in range(10):
+        args = (xs[:, t], Bs[:, t], Cs[:, t], dts[:, t])
+        y0, y1, y2 = plain.step(*args), counted.step(*args), zeroing.step(*args)
+        assert np.array_equal(y0, y1)
+        if t < 4:
+            assert np.array_equal(y0, y2)
+        if t == 3:
+            assert np.array_equal(zeroing.h, np.zeros_like(h0))
+    assert len(calls) == 2
+    assert np.array_equal(plain.h, counted.h)
+
+
+ALL_PINS.append(pin_window_rounding_only_at_window_ends)

@@ -12,7 +12,7 @@ def test_exports_every_header_symbol(lib):
     assert len(names) >= 17
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.replay_abi_version() == 1
+    assert lib.replay_abi_version() == 2
     assert lib.replay_strerror(-3) == b"capacity exceeded"
 
 
@@ -34,14 +34,22 @@ def test_layout_ring_capacity_and_read_copies():
     assert L.cap == 16 + 2 * 4 - 1
     assert L.scale - L.rc == 512 * 8 * 64 * 128
     assert L.xbuf - L.scale == 512 * 8 * 4
-    cfg.read_copy = R.REPLAY_RC_BF16
-    L = R.replay_layout_of(cfg)
-    assert L.scale - L.rc == 512 * 8 * 64 * 128 * 2 and L.xbuf == L.scale
+    for rc in (R.REPLAY_RC_BF16, R.REPLAY_RC_FP16):
+        cfg.read_copy = rc
+        L = R.replay_layout_of(cfg)
+        assert L.scale - L.rc == 512 * 8 * 64 * 128 * 2 and L.xbuf == L.scale
+
+
+def test_fp16_copy_has_no_dstate_256_kernel():
+    cfg = R.ReplayConfig(4, 8, 64, 256, 4, 16, 0, R.REPLAY_F32, R.REPLAY_RC_FP16, 1)
+    with pytest.raises(R.ReplayError) as e:
+        R.replay_layout_of(cfg)
+    assert e.value.code == -2
 
 
 @pytest.mark.parametrize("field,value,code", [
     ("batch", 0, -1), ("nheads", 6, -1), ("ngroups", 0, -1), ("window_L", 0, -1),
-    ("max_draft_T", -1, -1), ("in_dtype", 7, -1), ("read_copy", 3, -1), ("headdim", 48, -2),
+    ("max_draft_T", -1, -1), ("in_dtype", 7, -1), ("read_copy", 4, -1), ("headdim", 48, -2),
     ("dstate", 96, -2), ("window_L", 65, -3), ("max_draft_T", 9, -3)])
 def test_layout_rejects(field, value, code):
     cfg = R.ReplayConfig(4, 8, 64, 128, 4, 16, 2, R.REPLAY_F32, R.REPLAY_RC_NONE)
@@ -67,3 +75,15 @@ def test_calls_reject_null_arguments_before_cuda(lib):
     assert lib.conv_commit(4, 0, 256, 256, None, None) == -1
     bad = R.ReplayConfig(4, 8, 64, 96, 4, 16, 2, R.REPLAY_F32, R.REPLAY_RC_NONE)
     assert lib.conv_step(ctypes.byref(bad), 256, 0, 256, 256, 256, 256, 256, 256, 256, None) == -2
+
+
+def test_shared_checkpoint_layout_and_rules():
+    cfg = R.ReplayConfig(4, 8, 64, 128, 4, 16, 0, R.REPLAY_F32, R.REPLAY_RC_BF16, 1)
+    L = R.replay_layout_of(cfg)
+    assert L.h0 == 0 and L.rc == 0                 # no FP32 checkpoint region
+    assert L.scale - L.rc == 4 * 8 * 64 * 128 * 2
+    for rc, shared in ((R.REPLAY_RC_NONE, 1), (R.REPLAY_RC_BF16, 2)):
+        cfg = R.ReplayConfig(4, 8, 64, 128, 4, 16, 0, R.REPLAY_F32, rc, shared)
+        with pytest.raises(R.ReplayError) as e:
+            R.replay_layout_of(cfg)
+        assert e.value.code == -1

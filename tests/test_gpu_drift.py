@@ -1,15 +1,17 @@
 """Dual-precision drift over a long decode (GPU vs the FP64 oracle).
 
-The tiny layer's shape at batch 256 decodes 4096 tokens four ways on identical inputs:
+The tiny layer's shape at batch 256 decodes 4096 tokens seven ways on identical inputs:
 ReplaySSM with the FP32 checkpoint only, with a bf16 read copy, with an E4M3 read copy,
-and the conventional step with a bf16 stored state. The oracle follows four seeded
-sequences. Source: "ReplaySSM: Rethinking State Storage for Faster Hybrid-Model Decoding",
+with a shared bf16, E4M3 or FP16 (stochastically rounded) checkpoint (the copy is the
+recurrence state, rounded once per window and fed back), and the conventional step with a
+bf16 stored state. The oracle
+follows four seeded sequences. Source: "ReplaySSM: Rethinking State Storage for Faster Hybrid-Model Decoding",
 sections "State quantization" (a low-precision state's rounding re-enters the recurrence
 every step) and "Benefit 3" (a read copy's error stays within a window and does not grow).
 
 Checked: the FP32 path stays within 1e-4 throughout; the bf16 copy within 1e-2; the read
 copies' error does not grow with length (last quarter vs first quarter). Reported: the
-per-512-token max / mean of the per-vector relative error for all four paths (printed, and
+per-512-token max / mean of the per-vector relative error for all seven paths (printed, and
 written as JSON to $REPLAY_DRIFT_REPORT when that is set).
 """
 import json
@@ -41,6 +43,10 @@ def test_dual_precision_drift_4096_tokens():
               (("replay_fp32", R.REPLAY_RC_NONE), ("replay_bf16_copy", R.REPLAY_RC_BF16),
                ("replay_e4m3_copy", R.REPLAY_RC_FP8E4M3))}
     A, D = sg.head_params(shape.nheads, seed)
+    for name, rc in (("shared_bf16_checkpoint", R.REPLAY_RC_BF16), ("shared_e4m3_checkpoint", R.REPLAY_RC_FP8E4M3),
+                     ("shared_fp16_sr_checkpoint", R.REPLAY_RC_FP16)):
+        cfg_s = R.ReplayConfig(256, 8, 64, 128, 1, L, 0, R.REPLAY_F32, rc, 1)
+        stores[name] = R.ReplayStore(cfg_s, torch.from_numpy(A), torch.from_numpy(D))
     Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
     cfg = make_cfg(shape, L=L)
     state16 = torch.zeros(256, 8, 64, 128, device="cuda", dtype=torch.bfloat16)

@@ -55,6 +55,7 @@ def test_tiny_layer_all_steps():
     assert wy <= TOL and wh <= TOL, (wy, wh)
     meta = st.region("meta").cpu().numpy()
     assert meta[0, 1] == 0 and meta[0, 2] == 0           # 64 = 4 windows: ring empty
+    assert meta[0, 3] == 5                               # the load was write 0, then 4 flushes
 
 
 @pytest.mark.parametrize("N,dtype,G,L,steps", [
@@ -171,19 +172,31 @@ def test_read_copy_fp8_drift_is_bounded():
     assert wh <= TOL and wy <= 0.25, (wy, wh)
 
 
-@pytest.mark.parametrize("rc", [R.REPLAY_RC_BF16, R.REPLAY_RC_FP8E4M3])
-def test_read_copy_codes_match_format_definitions(rc):
+@pytest.mark.parametrize("rc,shared", [(R.REPLAY_RC_BF16, 0), (R.REPLAY_RC_FP8E4M3, 0),
+                                       (R.REPLAY_RC_FP16, 0), (R.REPLAY_RC_FP16, 1)])
+def test_read_copy_codes_match_format_definitions(rc, shared):
     """The copy written by a checkpoint write equals the format encoders applied to the
-    same FP32 state, bit for bit (codes decided in FP32 on both sides)."""
+    same FP32 state, bit for bit (codes decided in FP32 on both sides). A shared FP16
+    checkpoint is rounded stochastically with the draws of write number 0."""
     shape = sg.LayerShape(3, 4, 64, 128, 1, "f32")
-    st, _, _ = make_store(shape, 9, L=4, read_copy=rc)
+    A, D = sg.head_params(4, 9)
+    cfg = R.ReplayConfig(3, 4, 64, 128, 1, 4, 0, R.REPLAY_F32, rc, shared)
+    st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
     h = sg.initial_state(shape, 9)
     h[0, 1] = 0.0                                  # an all-zero slab: scale 1
     h[1, 2, 0, :4] = [1e-12, -3e-9, 500.0, -1e30]  # tiny, subnormal-range and huge values
+    h[2, 3, 5, :3] = [7e4, -65504.0, 3e-8]         # FP16: past the largest finite, at it, subnormal
     st.load_state(torch.from_numpy(h).cuda())
     got = st.region("rc").cpu()
     if rc == R.REPLAY_RC_BF16:
         assert np.array_equal(got.view(torch.int16).numpy().view(np.uint16), F.bf16_encode(h))
+    elif rc == R.REPLAY_RC_FP16 and not shared:
+        assert np.array_equal(got.view(torch.int16).numpy().view(np.uint16), F.fp16_encode(h))
+    elif rc == R.REPLAY_RC_FP16:
+        want = F.fp16_sr_round_state(h, 0, np.arange(3), 3 * 4)
+        assert np.array_equal(got.double().numpy(), want)
+        assert np.abs(want[2, 3, 5, 0]) == 65504.0          # saturated, not infinite
+        assert st.region("meta").cpu().numpy()[:, 3].tolist() == [1, 1, 1]
     else:
         scale = st.region("scale").cpu().numpy()
         for b in range(3):
@@ -292,3 +305,98 @@ def test_host_errors():
     with pytest.raises(R.ReplayError) as e:
         st.verify(0, *devs, y)
     assert e.value.code == -1
+
+
+def test_fused_and_split_step_paths_agree():
+    """Calls with few slabs take the single fused kernel, larger ones the per-group prep +
+    per-head kernels. The same sequences (inputs do not depend on the batch size) through
+    both paths -- 128 and 129 sequences x 64 heads straddle the threshold -- agree with each
+    other and with the oracle, across two flushes."""
+    outs = []
+    sel = np.array([0, 63, 127])
+    for batch in (128, 129):
+        shape = sg.LayerShape(batch, 64, 64, 128, 4, "bf16")
+        st, A, D = make_store(shape, 16, L=4)
+        orc = Mamba2Decoder(A, D, 4, np.zeros((3, 64, 64, 128)))
+        y = torch.empty(batch, 64, 64, device="cuda")
+        ys = []
+        for t in range(9):
+            devs, f64 = step_inputs(shape, 16, t, sel)
+            st.step(*devs, y)
+            assert rel_vec_err(y[sel].cpu().numpy(), orc.step(*f64), 2).max() <= TOL, (batch, t)
+            ys.append(y[:128].cpu().numpy().copy())
+        assert st.status() == 0
+        outs.append(np.stack(ys))
+    assert rel_vec_err(outs[1], outs[0], 3).max() <= 1e-5
+
+
+@pytest.mark.parametrize("rc,bound", [(R.REPLAY_RC_BF16, 1e-2), (R.REPLAY_RC_FP8E4M3, 0.25)])
+def test_read_copy_on_the_large_call_path(rc, bound):
+    """Above the fused-kernel threshold a read copy is read by CTAs that each take several
+    heads of a group (packed copy tiles). 72 sequences x 128 heads, 8 groups, across two
+    flushes; the oracle follows three sequences, and the FP32 checkpoints stay exact."""
+    shape = sg.LayerShape(72, 128, 64, 128, 8, "bf16")
+    wy, wh, _, _ = run_decode(shape, 18, 8, seed=17, read_copy=rc, seqs=[0, 35, 71])
+    assert wy <= bound and wh <= TOL, (wy, wh)
+
+
+class _SrRounder:
+    """FP16 stochastic rounding of the followed sequences, one epoch per call (the first
+    flush is write number 1; the load or reset was number 0)."""
+
+    def __init__(self, sel, num_slabs):
+        self.sel, self.num_slabs, self.epoch = sel, num_slabs, 1
+
+    def __call__(self, h):
+        out = F.fp16_sr_round_state(h, self.epoch, self.sel, self.num_slabs)
+        self.epoch += 1
+        return out
+
+
+@pytest.mark.parametrize("rc,tol", [(R.REPLAY_RC_BF16, 5e-3), (R.REPLAY_RC_FP8E4M3, 5e-2),
+                                    (R.REPLAY_RC_FP16, 1e-3)])
+@pytest.mark.parametrize("batch,heads,groups", [(4, 8, 2), (72, 128, 8)])
+def test_shared_checkpoint_matches_periodic_rounding(rc, tol, batch, heads, groups):
+    """With shared_checkpoint the low-precision copy is the recurrence state: every flush
+    starts from it and writes only it. The oracle rounds its FP64 state the same way after
+    every L-th token (FP16: stochastically, with the same draws). Outputs follow that oracle
+    (up to rare rounding flips between FP32 and FP64 states) and drift from the unrounded
+    one."""
+    shape = sg.LayerShape(batch, heads, 64, 128, groups, "f32")
+    L, steps, seed = 8, 40, 18
+    A, D = sg.head_params(heads, seed)
+    cfg = R.ReplayConfig(batch, heads, 64, 128, groups, L, 0, R.REPLAY_F32, rc, 1)
+    st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
+    sel = np.array([0, batch - 1])
+    rounder = {R.REPLAY_RC_BF16: F.bf16_round_state, R.REPLAY_RC_FP8E4M3: F.e4m3_round_state,
+               R.REPLAY_RC_FP16: _SrRounder(sel, batch * heads)}[rc]
+    z = np.zeros((2, heads, 64, 128))
+    rounded = Mamba2Decoder(A.astype(float), D.astype(float), groups, z, window_round=rounder, window_L=L)
+    plain = Mamba2Decoder(A.astype(float), D.astype(float), groups, z)
+    y = torch.empty(batch, heads, 64, device="cuda")
+    e_round = e_plain = 0.0
+    for t in range(steps):
+        devs, f64 = step_inputs(shape, seed, t, sel)
+        st.step(*devs, y)
+        yg = y[sel].cpu().numpy()
+        e_round = max(e_round, rel_vec_err(yg, rounded.step(*f64), 2).max())
+        e_plain = max(e_plain, rel_vec_err(yg, plain.step(*f64), 2).max())
+    h = torch.empty(batch, heads, 64, 128, device="cuda")
+    st.export_state(h)                     # the last step was a flush: h is the stored copy
+    hg = h.cpu().numpy()
+    # The checkpoint is the rounded state itself: every value lies on the format's grid.
+    if rc == R.REPLAY_RC_BF16:
+        assert not np.any(hg.view(np.uint32) & 0xFFFF)
+    elif rc == R.REPLAY_RC_FP16:
+        assert np.array_equal(hg, hg.astype(np.float16).astype(np.float32))
+    else:
+        scale = st.region("scale").cpu().numpy()[:, :, None, None]
+        assert np.array_equal(F.fp8_slab_dequantize(F.e4m3_encode(hg / scale), scale), hg)
+    # ... and follows the rounded oracle. FP32 and FP64 states can round a value that sits
+    # near a midpoint (or a scale) differently: such flips move one element by one code
+    # step and are rare; everything else agrees to FP32 accuracy.
+    step = {R.REPLAY_RC_BF16: 2.0 ** -7, R.REPLAY_RC_FP8E4M3: 32 / 448, R.REPLAY_RC_FP16: 2.0 ** -10}[rc]
+    d = np.abs(hg[sel] - rounded.h) / np.abs(rounded.h).max(axis=(2, 3), keepdims=True)
+    assert d.max() <= 2 * step and (d > 1e-5).mean() <= 1e-3, (d.max(), (d > 1e-5).mean())
+    assert e_round <= tol and e_plain > 2 * e_round, (e_round, e_plain)
+    assert st.status() == 0

@@ -99,3 +99,138 @@ def test_fp8_slab_scale_and_codes():
     assert np.all(np.abs(back[big] - h[big]) <= np.abs(h[big]) * 2.0 ** -4)
     z, s0 = F.fp8_slab_quantize(np.zeros((4, 4), np.float32))
     assert s0 == 1.0 and not np.any(z & 0x7F)
+
+
+def test_state_rounding_helpers():
+    rng = np.random.default_rng(5)
+    h = rng.standard_normal((2, 3, 4, 8))
+    hb = F.bf16_round_state(h)
+    assert np.array_equal(hb, F.bf16_decode(F.bf16_encode(h.astype(np.float32))))
+    he = F.e4m3_round_state(h)
+    for b in range(2):
+        for k in range(3):
+            q, s = F.fp8_slab_quantize(h[b, k].astype(np.float32))
+            assert np.array_equal(he[b, k], F.fp8_slab_dequantize(q, s))
+
+
+def test_fp16_code_points_roundtrip_and_ties():
+    assert F.fp16_decode(np.uint16(0x3C00)) == 1.0 and F.fp16_decode(np.uint16(0x7BFF)) == 65504.0
+    assert F.fp16_decode(np.uint16(0x0001)) == 2.0 ** -24 and F.fp16_decode(np.uint16(0x0400)) == 2.0 ** -14
+    assert np.isinf(F.fp16_decode(np.uint16(0x7C00))) and np.isnan(F.fp16_decode(np.uint16(0x7E00)))
+    p = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    finite = p[((p.astype(np.uint32) >> 10) & 0x1F) != 0x1F]
+    assert np.array_equal(F.fp16_encode(F.fp16_decode(finite).astype(np.float32)), finite)
+    pos = np.arange(0x7C00, dtype=np.uint16)
+    v = F.fp16_decode(pos)
+    mid = ((v[:-1] + v[1:]) / 2).astype(np.float32)        # exact in FP32
+    even = np.where(pos[:-1] & 1, pos[:-1] + 1, pos[:-1]).astype(np.uint16)
+    assert np.array_equal(F.fp16_encode(mid), even)
+    assert F.fp16_encode(np.float32(65520.0)) == 0x7C00    # midpoint past 65504 -> inf
+    assert F.fp16_encode(np.float32(65519.0)) == 0x7BFF
+
+
+def test_fp16_stochastic_rounding_definition():
+    lo_hi = F.fp16_decode(np.array([0x3C00, 0x3C01], dtype=np.uint16))   # 1 and 1 + 2**-10
+    v = np.float32(1.0 + 0.25 * 2.0 ** -10)                               # a quarter of the way
+    assert F.fp16_sr_encode(v, 0.0) == 0x3C01 and F.fp16_sr_encode(v, 0.2499) == 0x3C01
+    assert F.fp16_sr_encode(v, 0.25) == 0x3C00 and F.fp16_sr_encode(v, 0.9) == 0x3C00
+    assert F.fp16_sr_encode(-v, 0.1) == 0xBC01                            # sign kept
+    exact = F.fp16_decode(np.arange(0, 0x7C00, 97, dtype=np.uint16)).astype(np.float32)
+    assert np.array_equal(F.fp16_decode(F.fp16_sr_encode(exact, 0.0)), exact)   # no bias on grid points
+    assert F.fp16_sr_encode(np.float32(1e6), 0.0) == 0x7BFF                     # saturates
+    # unbiased: the mean over uniform draws is the value itself
+    u = F.sr_uniform(np.arange(200000, dtype=np.uint64))
+    assert abs(u.mean() - 0.5) < 0.003 and u.min() >= 0 and u.max() < 1
+    vals = F.fp16_decode(F.fp16_sr_encode(np.full(200000, 1.0 + 0.3 * 2.0 ** -10, np.float32), u))
+    assert abs(vals.mean() - (1.0 + 0.3 * 2.0 ** -10)) < 2e-6
+    assert set(np.unique(vals)) <= set(lo_hi)
+
+
+def test_splitmix64_reference_values():
+    """The first outputs of the published generator started at 0."""
+    z = F.splitmix64(0, np.arange(3))
+    assert [int(v) for v in z] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    assert F.sr_uniform(np.array([5]))[0] == (int(F.splitmix64(F.SR_SEED, [5])[0]) >> 40) / 2.0 ** 24
+
+
+# ------------------------------------------------------------------ NVFP4
+# The E2M1 value set as the format's published tables list it (codes 0..7; 8..15 are the
+# negatives): 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_code_points_and_roundtrip():
+    codes = np.arange(16, dtype=np.uint8)
+    want = np.array(E2M1_TABLE + [-v for v in E2M1_TABLE])
+    got = F.e2m1_decode(codes)
+    assert np.array_equal(got, want)
+    assert np.all(np.signbit(got[8:]))                       # code 8 is -0
+    assert np.array_equal(F.e2m1_encode(got.astype(np.float32)), codes)
+
+
+def test_e2m1_ties_to_even_nearest_and_saturation():
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], dtype=np.float32)
+    want = [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0]               # the neighbour with fraction bit 0
+    assert F.e2m1_decode(F.e2m1_encode(mids)).tolist() == want
+    assert F.e2m1_decode(F.e2m1_encode(-mids)).tolist() == [-w for w in want]
+    near = np.array([0.26, 0.74, 1.3, 2.49, 2.51, 3.4, 4.9, 5.1, 6.0, 7.0, 1e30], dtype=np.float32)
+    assert F.e2m1_decode(F.e2m1_encode(near)).tolist() == [0.5, 0.5, 1.5, 2.0, 3.0, 3.0, 4.0, 6.0, 6.0, 6.0, 6.0]
+    assert F.e2m1_encode(np.float32(-1e-9)) == 0x8              # sign kept on zero
+
+
+def test_nvfp4_pack_nibble_order():
+    q = np.array([[2, 7, 0, 15]], dtype=np.uint8)               # 1.0, 6.0, 0, -6.0
+    b = F.nvfp4_pack(q)
+    assert b.tolist() == [[0x72, 0xF0]]
+    assert np.array_equal(F.nvfp4_unpack(b), q)
+
+
+def test_nvfp4_exactly_representable_slab():
+    """A slab built from E2M1 values times block scales that E4M3 holds exactly, with the
+    slab's absmax 448 * 6 * s_g: every code comes back exactly and every value to FP32
+    rounding."""
+    rng = np.random.default_rng(3)
+    P, N = 8, 64
+    s_g = np.float32(1.0 / 4096)                              # a power of two: products exact
+    bs_vals = F.e4m3_decode(np.arange(0x38, 0x7F, dtype=np.uint8))   # 1 .. 448
+    s_b = rng.choice(bs_vals, size=(P, N // 16))
+    s_b[0, 0] = 448.0
+    k = rng.integers(0, 16, size=(P, N)).astype(np.uint8)
+    k[0, 0] = 7                                              # the slab's absmax: 6 * 448 * s_g
+    for blk in np.ndindex(P, N // 16):                       # each block reaches +-6 once
+        k[blk[0], blk[1] * 16] = 7
+    h = (F.e2m1_decode(k).reshape(P, N // 16, 16) * (s_b * s_g)[:, :, None]).reshape(P, N)
+    q, sb, sg = F.nvfp4_slab_quantize(h.astype(np.float32))
+    assert sg == s_g
+    assert np.array_equal(F.e4m3_decode(sb), s_b)
+    assert np.array_equal(F.e2m1_decode(q), F.e2m1_decode(k))
+    assert np.array_equal(F.nvfp4_slab_dequantize(q, sb, sg), h)
+
+
+def test_nvfp4_zero_slab_and_zero_block():
+    q, sb, sg = F.nvfp4_slab_quantize(np.zeros((4, 32), np.float32))
+    assert sg == 1.0 and not q.any() and not sb.any()
+    h = np.zeros((4, 32), np.float32)
+    h[0, 0] = 1.0
+    h[1, 17] = 1e-9                                          # far below the block-scale range
+    q, sb, sg = F.nvfp4_slab_quantize(h)
+    assert sb[1, 1] == 0 and not q[1, 16:].any()              # a zero scale zeroes the block
+    assert F.e2m1_decode(q[0, 0]) == 6.0 and F.e4m3_decode(sb[0, 0]) == 448.0
+
+
+def test_nvfp4_error_bound_on_random_slabs():
+    """Each value read back is within one E2M1 step of the block's scale unit e (the
+    largest half step, between 4 and 6, is 1 * e), and a block's absmax within 1/8 of
+    itself (a normal E4M3 scale is within 2**-4 of exact, then E2M1 saturates at 6; these
+    Gaussian slabs keep every block scale in the normal range)."""
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        h = (rng.standard_normal((16, 128)) * 10.0 ** rng.uniform(-6, 3)).astype(np.float32)
+        q, sb, sg = F.nvfp4_slab_quantize(h)
+        e = F.e4m3_decode(sb) * float(sg)
+        back = F.nvfp4_slab_dequantize(q, sb, sg)
+        err = np.abs(back - h).reshape(16, 8, 16)
+        assert np.all(err <= e[:, :, None] * (1.0 + 1e-6)), trial
+        bmax = np.abs(h).reshape(16, 8, 16).max(axis=2)
+        bback = np.abs(back).reshape(16, 8, 16).max(axis=2)
+        assert np.all(np.abs(bback - bmax) <= bmax / 8 + 1e-30), trial

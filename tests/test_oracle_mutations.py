@@ -85,3 +85,68 @@ def test_commit_off_by_one_is_caught(monkeypatch):
 
 def test_unmutated_oracle_passes_all_pins():
     assert _fails_some_pin() is None
+
+
+# ------------------------------------------------------------------ storage formats
+import oracle.formats as fm  # noqa: E402
+import test_oracle_formats as fmt_pins  # noqa: E402
+
+FORMAT_PINS = [getattr(fmt_pins, n) for n in dir(fmt_pins) if n.startswith("test_")]
+
+
+def _format_pin_fails():
+    for pin in FORMAT_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            return pin.__name__
+    return None
+
+
+def _e2m1_ties_away(v):
+    f = np.asarray(v, dtype=np.float32).astype(np.float64)
+    a = np.abs(f)
+    d = np.abs(a[..., None] - fm._E2M1_POS)
+    code = np.where(d == d.min(axis=-1, keepdims=True), np.arange(8), -1).max(axis=-1)   # larger on ties
+    return (code | np.where(np.signbit(f), 0x8, 0)).astype(np.uint8)
+
+
+def _pack_swapped(q):
+    q = np.asarray(q, dtype=np.uint8)
+    return ((q[..., 0::2] & 0xF) << 4) | (q[..., 1::2] & 0xF)
+
+
+def _slab_scale_without_e2m1_max(h):
+    h = np.asarray(h, dtype=np.float32)
+    P, N = h.shape
+    absmax = np.float32(np.max(np.abs(h)))
+    s_g = np.float32(1.0) if absmax == 0 else np.float32(absmax / np.float32(fm.E4M3_MAX))
+    blocks = h.reshape(P, N // 16, 16)
+    s_b = fm.e4m3_encode((np.max(np.abs(blocks), axis=2) / (np.float32(6.0) * s_g)).astype(np.float32))
+    e = (fm.e4m3_decode(s_b).astype(np.float32) * s_g).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(e[:, :, None] > 0, fm.e2m1_encode((blocks / e[:, :, None]).astype(np.float32)), 0)
+    return q.reshape(P, N).astype(np.uint8), s_b, s_g
+
+
+def _sr_round_to_nearest(v, u):
+    return fm.fp16_encode(v)
+
+
+FORMAT_MUTATIONS = {
+    "e2m1_ties_away_from_zero": ("e2m1_encode", _e2m1_ties_away),
+    "nvfp4_nibbles_swapped": ("nvfp4_pack", _pack_swapped),
+    "nvfp4_slab_scale_missing_6": ("nvfp4_slab_quantize", _slab_scale_without_e2m1_max),
+    "fp16_sr_is_round_to_nearest": ("fp16_sr_encode", _sr_round_to_nearest),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FORMAT_MUTATIONS))
+def test_planted_format_mistake_is_caught(name, monkeypatch):
+    attr, fn = FORMAT_MUTATIONS[name]
+    monkeypatch.setattr(fm, attr, fn)
+    assert _format_pin_fails() is not None, f"no pin catches {name}"
+
+
+def test_unmutated_formats_pass_all_pins():
+    assert _format_pin_fails() is None

@@ -69,7 +69,8 @@ def test_rejects_batch_beyond_the_limit(lib):
     st, _, _ = make_store(shape, 32, L=2)
     devs, _ = step_inputs(shape, 32, 0)
     y = torch.zeros(limit + 1, 1, 64, device="cuda")
+    meta_before = st.region("meta").clone()
     assert _c_call(lib, st, devs, y) == -3            # REPLAY_ECAPACITY, nothing launched
     torch.cuda.synchronize()
     assert not torch.any(y != 0)
-    assert np.all(st.region("meta").cpu().numpy() == 0)
+    assert torch.equal(st.region("meta"), meta_before)
