@@ -43,7 +43,12 @@ def record_bytes(w, esz):
     return (w["nheads"] * w["headdim"] + w["ngroups"] * w["dstate"] + w["nheads"]) * esz
 
 
-def step_bytes(w, n_prior: int, flush: bool, esz=2, state_bytes=4, rc_bytes=0, shared=False):
+# Read-copy bytes per state element (NVFP4: half a byte of code plus one E4M3 scale per 16)
+# and whether the copy has an FP32 scale per slab.
+RC_BYTES = {"bf16": (2, False), "e4m3": (1, True), "fp16": (2, False), "nvfp4": (0.5 + 1 / 16, True)}
+
+
+def step_bytes(w, n_prior: int, flush: bool, esz=2, state_bytes=4, rc_bytes=0, shared=False, slab_scale=False):
     """Algorithmic HBM bytes of one replay_step launch over the batch.
 
     Reads: the checkpoint (FP32, or the read copy on a non-flush step), the n_prior
@@ -56,12 +61,12 @@ def step_bytes(w, n_prior: int, flush: bool, esz=2, state_bytes=4, rc_bytes=0, s
     rec = b * record_bytes(w, esz)
     inputs = b * (H * P + 2 * G * N + H) * esz
     y = b * H * P * 4
+    copy = S * rc_bytes + (b * H * 4 if slab_scale else 0)
     if flush:
-        scale = b * H * 4 if rc_bytes == 1 else 0
         if shared:
-            return 2 * (S * rc_bytes + scale) + n_prior * rec + inputs + y
-        return S * state_bytes + n_prior * rec + inputs + y + S * (state_bytes + rc_bytes) + scale
-    read = S * (rc_bytes if rc_bytes else state_bytes) + (b * H * 4 if rc_bytes == 1 else 0)
+            return 2 * copy + n_prior * rec + inputs + y
+        return S * state_bytes + n_prior * rec + inputs + y + S * state_bytes + copy
+    read = copy if rc_bytes else S * state_bytes
     return read + n_prior * rec + inputs + y + rec
 
 
@@ -205,8 +210,10 @@ def run_replay(args, rank, world, local_rank):
     L = w["L"]
     shape = sg.LayerShape(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["dtype"])
     A, D = sg.head_params(w["nheads"], 0)
+    rc_code = {"none": R.REPLAY_RC_NONE, "bf16": R.REPLAY_RC_BF16, "e4m3": R.REPLAY_RC_FP8E4M3,
+               "fp16": R.REPLAY_RC_FP16, "nvfp4": R.REPLAY_RC_NVFP4}[args.read_copy]
     cfg = R.ReplayConfig(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], L, 0,
-                         R.REPLAY_BF16, R.REPLAY_RC_NONE)
+                         R.REPLAY_BF16, rc_code, int(args.shared_checkpoint))
     st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
     dev, host = window_inputs(shape, rank, L, torch)
     y = torch.empty(w["batch"], w["nheads"], w["headdim"], device="cuda")
@@ -244,7 +251,9 @@ def run_replay(args, rank, world, local_rank):
     tokens = world * w["batch"] * L * args.steps
 
     # roofline of replay_step: algorithmic bytes of every launch / its event-timed duration
-    per_pos = [step_bytes(w, t, flush=(t == L - 1)) for t in range(L)]
+    rcb, slab_scale = RC_BYTES[args.read_copy] if args.read_copy != "none" else (0, False)
+    per_pos = [step_bytes(w, t, flush=(t == L - 1), rc_bytes=rcb, shared=args.shared_checkpoint,
+                          slab_scale=slab_scale) for t in range(L)]
     alg_bytes = sum(per_pos) * args.steps
     kern_s = launch_s.sum()
     peak, peak_kind = hbm_peak()
@@ -252,6 +261,11 @@ def run_replay(args, rank, world, local_rank):
     nf_bytes = sum(per_pos[:-1]) * args.steps
     nf_s = launch_s[:, :-1].sum()
     traffic = recorded_traffic()
+    if args.kernels_only:   # a short diagnostic line for profiling runs, not the benchmark line
+        return {"mode": "kernels-only", "read_copy": args.read_copy, "shared_checkpoint": args.shared_checkpoint,
+                "tokens_per_s": tokens / elapsed_max, "achieved_gbs": achieved,
+                "nonflush_launch_us": float(launch_s[:, :-1].mean() * 1e6),
+                "flush_launch_us": float(launch_s[:, -1].mean() * 1e6)}
 
     # e2e: every token's inputs come from pinned host memory and its y goes back to pinned
     # host memory, through the public call. Copies run on their own streams, double-buffered,
@@ -327,6 +341,9 @@ def run_replay(args, rank, world, local_rank):
     extra = {}
     if not args.no_extra:
         extra["read_copy"] = run_read_copies(torch, R, dev)
+        fp32_nf_us = float(launch_s[:, :-1].mean() * 1e6)
+        for v in extra["read_copy"].values():   # the post's "non-flush kernel N x faster" figure
+            v["nonflush_speedup_vs_fp32"] = fp32_nf_us / v["nonflush_launch_us"]
         extra["speculative"] = run_speculative(torch, R)
 
     result = {
@@ -445,10 +462,13 @@ def run_read_copies(torch, R, dev, steps=10):
     A, D = sg.head_params(w["nheads"], 0)
     y = torch.empty(w["batch"], w["nheads"], w["headdim"], device="cuda")
     out = {}
-    for name, rc, rcb, shared in (("bf16", R.REPLAY_RC_BF16, 2, 0), ("e4m3", R.REPLAY_RC_FP8E4M3, 1, 0),
-                                  ("fp16", R.REPLAY_RC_FP16, 2, 0), ("shared_bf16", R.REPLAY_RC_BF16, 2, 1),
-                                  ("shared_e4m3", R.REPLAY_RC_FP8E4M3, 1, 1),
-                                  ("shared_fp16_sr", R.REPLAY_RC_FP16, 2, 1)):
+    for name, rc, fmt, shared in (("bf16", R.REPLAY_RC_BF16, "bf16", 0), ("e4m3", R.REPLAY_RC_FP8E4M3, "e4m3", 0),
+                                  ("fp16", R.REPLAY_RC_FP16, "fp16", 0), ("nvfp4", R.REPLAY_RC_NVFP4, "nvfp4", 0),
+                                  ("shared_bf16", R.REPLAY_RC_BF16, "bf16", 1),
+                                  ("shared_e4m3", R.REPLAY_RC_FP8E4M3, "e4m3", 1),
+                                  ("shared_fp16_sr", R.REPLAY_RC_FP16, "fp16", 1),
+                                  ("shared_nvfp4", R.REPLAY_RC_NVFP4, "nvfp4", 1)):
+        rcb, slab_scale = RC_BYTES[fmt]
         cfg = R.ReplayConfig(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], L, 0,
                              R.REPLAY_BF16, rc, shared)
         st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
@@ -464,8 +484,8 @@ def run_read_copies(torch, R, dev, steps=10):
                 ev[k * L + t][1].record()
         torch.cuda.synchronize()
         us = np.array([a.elapsed_time(b) for a, b in ev]).reshape(steps, L) * 1e3
-        nf_bytes = sum(step_bytes(w, t, False, rc_bytes=rcb) for t in range(L - 1))
-        fl_bytes = step_bytes(w, L - 1, True, rc_bytes=rcb, shared=bool(shared))
+        nf_bytes = sum(step_bytes(w, t, False, rc_bytes=rcb, slab_scale=slab_scale) for t in range(L - 1))
+        fl_bytes = step_bytes(w, L - 1, True, rc_bytes=rcb, shared=bool(shared), slab_scale=slab_scale)
         out[name] = {"tokens_per_s": w["batch"] * L / (us.sum(axis=1).mean() * 1e-6),
                      "nonflush_launch_us": float(us[:, :-1].mean()),
                      "flush_launch_us": float(us[:, -1].mean()),
@@ -615,6 +635,12 @@ def main(argv=None):
     ap.add_argument("--cpu-sample-tokens", type=int, default=48)
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary workloads (read copies, speculative verify)")
+    ap.add_argument("--read-copy", default="none", choices=["none", "bf16", "e4m3", "fp16", "nvfp4"],
+                    help="diagnostics: give the timed store this read copy (the benchmark line is 'none')")
+    ap.add_argument("--shared-checkpoint", action="store_true",
+                    help="diagnostics: the read copy is the checkpoint (needs --read-copy)")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="diagnostics: time only the replay windows and print a short line (for ncu runs)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line: batch x window sweep and 40-layer stack, "
                          "one JSON line per configuration")

@@ -57,8 +57,9 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   int rc = check_shape(c);
   if (rc != REPLAY_OK) return rc;
   if (c->window_L < 1 || c->max_draft_T < 0) return REPLAY_EBADARG;
-  if (c->read_copy < REPLAY_RC_NONE || c->read_copy > REPLAY_RC_FP16) return REPLAY_EBADARG;
+  if (c->read_copy < REPLAY_RC_NONE || c->read_copy > REPLAY_RC_NVFP4) return REPLAY_EBADARG;
   if (c->read_copy == REPLAY_RC_FP16 && c->dstate > 128) return REPLAY_EUNSUPPORTED;
+  if (c->read_copy == REPLAY_RC_NVFP4 && c->dstate != 128) return REPLAY_EUNSUPPORTED;
   if (c->shared_checkpoint != 0 && (c->shared_checkpoint != 1 || c->read_copy == REPLAY_RC_NONE))
     return REPLAY_EBADARG;
   if (c->max_draft_T > 8) return REPLAY_ECAPACITY;
@@ -67,7 +68,11 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   if (cap > rssm::kMaxCap) return REPLAY_ECAPACITY;
   const size_t Bn = c->batch, H = c->nheads, G = c->ngroups, P = c->headdim, N = c->dstate;
   const size_t esz = c->in_dtype == REPLAY_F32 ? 4 : 2;
-  const size_t rcsz = c->read_copy == REPLAY_RC_NONE ? 0 : (c->read_copy == REPLAY_RC_FP8E4M3 ? 1 : 2);
+  // read-copy bytes per 2 elements
+  const size_t rc2 = c->read_copy == REPLAY_RC_NONE    ? 0
+                     : c->read_copy == REPLAY_RC_NVFP4 ? 1
+                     : c->read_copy == REPLAY_RC_FP8E4M3 ? 2 : 4;
+  const bool slab_scale = c->read_copy == REPLAY_RC_FP8E4M3 || c->read_copy == REPLAY_RC_NVFP4;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -77,8 +82,9 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   replay_layout L;
   L.cap = static_cast<int>(cap);
   L.h0 = take(c->shared_checkpoint ? 0 : Bn * H * P * N * 4);  // no FP32 checkpoint when shared
-  L.rc = take(Bn * H * P * N * rcsz);
-  L.scale = take(c->read_copy == REPLAY_RC_FP8E4M3 ? Bn * H * 4 : 0);
+  L.rc = take(Bn * H * P * N / 2 * rc2);
+  L.scale = take(slab_scale ? Bn * H * 4 : 0);
+  L.bscale = take(c->read_copy == REPLAY_RC_NVFP4 ? Bn * H * P * N / 16 : 0);
   L.xbuf = take(Bn * H * cap * P * esz);
   L.bbuf = take(Bn * G * cap * N * esz);
   L.dtbuf = take(Bn * H * cap * esz);
@@ -117,6 +123,7 @@ int replay_alloc(const replay_config* c, void* workspace, size_t workspace_bytes
   sv.h0 = reinterpret_cast<float*>(st->ws + L.h0);
   sv.rc = st->ws + L.rc;
   sv.scale = reinterpret_cast<float*>(st->ws + L.scale);
+  sv.bscale = reinterpret_cast<uint8_t*>(st->ws + L.bscale);
   sv.xbuf = st->ws + L.xbuf;
   sv.bbuf = st->ws + L.bbuf;
   sv.dtbuf = st->ws + L.dtbuf;
@@ -157,12 +164,16 @@ int replay_reset(replay_store* st, const int* seq_mask, void* stream) {
     int rc = cuda_ok(cudaMemsetAsync(st->sv.status, 0, sizeof(int), as_stream(stream)));
     if (rc != REPLAY_OK) return rc;
   }
-  return rssm::launch_load(st->sv, st->sh, nullptr, seq_mask, as_stream(stream));
+  const int rc = rssm::launch_load(st->sv, st->sh, nullptr, seq_mask, as_stream(stream));
+  st->all_n = rc == REPLAY_OK && seq_mask == nullptr ? 0 : -1;
+  return rc;
 }
 
 int replay_load_state(replay_store* st, const float* h, void* stream) {
   if (st == nullptr || h == nullptr) return REPLAY_EBADARG;
-  return rssm::launch_load(st->sv, st->sh, h, nullptr, as_stream(stream));
+  const int rc = rssm::launch_load(st->sv, st->sh, h, nullptr, as_stream(stream));
+  st->all_n = rc == REPLAY_OK ? 0 : -1;
+  return rc;
 }
 
 int replay_export_state(replay_store* st, float* h_out, void* stream) {
@@ -175,7 +186,9 @@ int replay_step(replay_store* st, const void* x, const void* B, const void* C, c
   if (st == nullptr || x == nullptr || B == nullptr || C == nullptr || dt == nullptr || y == nullptr)
     return REPLAY_EBADARG;
   if (!aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
-  return rssm::launch_step(st->sv, st->sh, x, B, C, dt, y, as_stream(stream));
+  const int rc = rssm::launch_step(st->sv, st->sh, st->all_n, x, B, C, dt, y, as_stream(stream));
+  if (rc == REPLAY_OK) st->all_n = advance_all_n(st);
+  return rc;
 }
 
 int replay_verify(replay_store* st, int T, const void* x, const void* B, const void* C,
@@ -184,17 +197,21 @@ int replay_verify(replay_store* st, int T, const void* x, const void* B, const v
     return REPLAY_EBADARG;
   if (T < 1 || !aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
   if (T > st->cfg.max_draft_T) return REPLAY_ECAPACITY;
+  st->all_n = -1;
   return rssm::launch_verify(st->sv, st->sh, T, x, B, C, dt, y, as_stream(stream));
 }
 
 int replay_commit(replay_store* st, const int* accept, void* stream) {
   if (st == nullptr || accept == nullptr) return REPLAY_EBADARG;
+  st->all_n = -1;
   return rssm::launch_commit(st->sv, accept, as_stream(stream));
 }
 
 int replay_flush(replay_store* st, void* stream) {
   if (st == nullptr) return REPLAY_EBADARG;
-  return rssm::launch_fold(st->sv, st->sh, 0, nullptr, as_stream(stream));
+  const int rc = rssm::launch_fold(st->sv, st->sh, 0, nullptr, as_stream(stream));
+  if (rc == REPLAY_OK) st->all_n = 0;
+  return rc;
 }
 
 int replay_status(replay_store* st, int* status_out, int clear, void* stream) {

@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -30,7 +31,8 @@ using bf16 = __nv_bfloat16;
 struct StoreView {
   float* h0;      // [batch][H][P][N]
   void* rc;       // read copy, bf16, e4m3 or fp16 [batch][H][P][N]
-  float* scale;   // [batch][H] (e4m3 copy)
+  float* scale;   // [batch][H] (e4m3 and nvfp4 copies)
+  uint8_t* bscale;  // [batch][H][P][N/16] e4m3 block scales (nvfp4 copy)
   void* xbuf;     // [batch][H][cap][P]
   void* bbuf;     // [batch][G][cap][N]
   void* dtbuf;    // [batch][H][cap]
@@ -160,6 +162,34 @@ __device__ __forceinline__ void st_e4m3_stream(uint8_t* p, float scale, const fl
     __stcs(reinterpret_cast<unsigned short*>(p), c);
   }
 }
+
+// NVFP4 copies (dstate 128): E2M1 codes, one E4M3 scale per 16 consecutive elements of a row
+// ([P][N/16], row-major), one FP32 scale per slab. Code layout of a row (64 bytes): quarter q
+// (0..3) of every block holds columns 4q..4q+3 of the block; the 8 blocks' quarter-q units sit
+// together at bytes 16q + 2b, 16q + 2b + 1. A unit's byte 0 holds columns 4q (slot A) and
+// 4q + 2 (slot B), byte 1 columns 4q + 1 (A) and 4q + 3 (B). Slot A keeps a code's sign in
+// bit 7 and its magnitude in bits 3..1, slot B the sign in bit 0 and the magnitude in bits
+// 6..4. So a lane that owns a row's quarter reads all 8 blocks of it with one 16-byte load,
+// and slot A is already the high byte of an FP16 equal to the E2M1 value times 2^-14.
+constexpr float kE2M1Max = 6.0f;
+constexpr int kFp4Block = 16;
+__device__ __forceinline__ float2 e2m1x2_to_float2(unsigned int byte) {
+  const __half2_raw r = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(byte & 0xffu), __NV_E2M1);
+  return __half22float2(*reinterpret_cast<const __half2*>(&r));
+}
+__device__ __forceinline__ unsigned int float2_to_e2m1x2(float a, float b) {
+  return __nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
+}
+__device__ __forceinline__ float e4m3_to_float(unsigned int code) {
+  return e4m3x2_to_float2(static_cast<unsigned short>(code & 0xffu)).x;
+}
+// E2M1 code (sign bit 3, magnitude bits 2..0) <-> the two byte slots
+__device__ __forceinline__ unsigned int fp4_slot_a(unsigned int c) { return ((c & 8u) << 4) | ((c & 7u) << 1); }
+__device__ __forceinline__ unsigned int fp4_slot_b(unsigned int c) { return ((c & 8u) >> 3) | ((c & 7u) << 4); }
+__device__ __forceinline__ unsigned int fp4_code_a(unsigned int byte) { return ((byte >> 4) & 8u) | ((byte >> 1) & 7u); }
+__device__ __forceinline__ unsigned int fp4_code_b(unsigned int byte) { return ((byte & 1u) << 3) | ((byte >> 4) & 7u); }
+// Byte offset of the unit of row `row`, block `b`, quarter `q` inside a slab's codes.
+__device__ __forceinline__ int fp4_unit(int row, int b, int q) { return row * 64 + q * 16 + b * 2; }
 
 // Read-copy "packs": the raw bytes of VEC consecutive copy elements, kept packed in registers
 // until they are used (so a thread can hold several heads' tiles), and their widening.
@@ -322,7 +352,8 @@ __device__ __forceinline__ unsigned short f16_sr(float v, float u) {
 // Read-copy tile loads/stores. RC is REPLAY_RC_BF16, REPLAY_RC_FP8E4M3 or REPLAY_RC_FP16.
 template <int P, int N, int RC>
 __device__ __forceinline__ void load_tile_rc(const void* rc, size_t slab, float scale, int warp,
-                                             int lane, float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+                                             int lane, float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E],
+                                             const uint8_t* bscale = nullptr) {
   using TL = Tile<P, N>;
 #pragma unroll
   for (int i = 0; i < TL::RPW; ++i)
@@ -330,7 +361,21 @@ __device__ __forceinline__ void load_tile_rc(const void* rc, size_t slab, float 
     for (int v = 0; v < TL::NVEC; ++v) {
       float t[TL::VEC];
       const size_t off = slab * P * N + TL::row(warp, i) * N + TL::col(lane, v);
-      if constexpr (RC == REPLAY_RC_BF16)
+      if constexpr (RC == REPLAY_RC_NVFP4) {
+        // the lane's 4 columns are one unit (block lane / 4, quarter lane % 4); value =
+        // decode(q) * (s_b * s_g)
+        static_assert(N == 128 && TL::VEC == 4, "the NVFP4 copy is laid out for dstate 128");
+        const float es = __fmul_rn(e4m3_to_float(__ldcs(bscale + off / kFp4Block)), scale);
+        const unsigned int u = __ldcs(reinterpret_cast<const unsigned short*>(
+            static_cast<const uint8_t*>(rc) + slab * P * N / 2 + fp4_unit(TL::row(warp, i), lane >> 2, lane & 3)));
+        const unsigned int b0 = u & 0xffu, b1 = u >> 8;
+        const float2 f01 = e2m1x2_to_float2(fp4_code_a(b0) | (fp4_code_a(b1) << 4));
+        const float2 f23 = e2m1x2_to_float2(fp4_code_b(b0) | (fp4_code_b(b1) << 4));
+        t[0] = f01.x * es;
+        t[1] = f01.y * es;
+        t[2] = f23.x * es;
+        t[3] = f23.y * es;
+      } else if constexpr (RC == REPLAY_RC_BF16)
         ld_bf16_stream<TL::VEC>(static_cast<const bf16*>(rc) + off, t);
       else if constexpr (RC == REPLAY_RC_FP16)
         ld_f16_stream<TL::VEC>(static_cast<const __half*>(rc) + off, t);
@@ -360,6 +405,39 @@ __device__ __forceinline__ void store_tile_rc(void* rc, size_t slab, float scale
       else
         st_e4m3_stream<TL::VEC>(static_cast<uint8_t*>(rc) + off, scale, t);
     }
+}
+
+// An NVFP4 tile with slab scale sg: each 16-element block of a row (4 consecutive lanes)
+// takes s_b = e4m3(block absmax / (6 sg)) and codes e2m1(h / (s_b sg)), every step one FP32
+// operation; a block whose scale is 0 stores zero codes. Lane l's 4 columns are the unit of
+// block l / 4, quarter l % 4 (layout above).
+template <int P, int N>
+__device__ __forceinline__ void store_tile_nvfp4(void* rc, uint8_t* bscale, size_t slab, float sg, int warp,
+                                                 int lane, const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+  static_assert(N == 128 && TL::VEC == 4 && TL::NVEC == 1, "the NVFP4 copy is laid out for dstate 128");
+  const float unit = __fmul_rn(kE2M1Max, sg);
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i) {
+    const float* t = hv[i];
+    float bm = fmaxf(fmaxf(fabsf(t[0]), fabsf(t[1])), fmaxf(fabsf(t[2]), fabsf(t[3])));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+    const unsigned int sb = float2_to_e4m3x2(__fdiv_rn(bm, unit), 0.f) & 0xffu;
+    const float es = __fmul_rn(e4m3_to_float(sb), sg);
+    unsigned int c01 = 0, c23 = 0;  // E2M1 codes of columns (0, 1) and (2, 3), low nibble first
+    if (es > 0.f) {
+      c01 = float2_to_e2m1x2(__fdiv_rn(t[0], es), __fdiv_rn(t[1], es));
+      c23 = float2_to_e2m1x2(__fdiv_rn(t[2], es), __fdiv_rn(t[3], es));
+    }
+    const unsigned int b0 = fp4_slot_a(c01 & 15u) | fp4_slot_b(c23 & 15u);
+    const unsigned int b1 = fp4_slot_a(c01 >> 4) | fp4_slot_b(c23 >> 4);
+    const int row = TL::row(warp, i);
+    __stcs(reinterpret_cast<unsigned short*>(static_cast<uint8_t*>(rc) + slab * P * N / 2 +
+                                             fp4_unit(row, lane >> 2, lane & 3)),
+           static_cast<unsigned short>(b0 | (b1 << 8)));
+    if ((lane & 3) == 0) __stcs(bscale + (slab * P + row) * (N / kFp4Block) + (lane >> 2), static_cast<uint8_t>(sb));
+  }
 }
 
 // An FP16 tile by stochastic rounding: element e of slab `slab` (of num_slabs) written by
@@ -489,6 +567,11 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+// cp.async groups: commit the copies issued so far as one group; wait until at most N groups
+// are still in flight.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 // Programmatic dependent launch: a primary kernel lets its dependent start early; the
 // dependent waits, where it first needs the primary's results, until the primary grid has

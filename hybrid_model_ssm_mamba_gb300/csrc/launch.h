@@ -16,7 +16,7 @@ struct Shape {
 };
 
 // Every (dstate, input type, read copy) combination with a kernel; headdim is 64. The FP16
-// copy has kernels for dstate 64 and 128.
+// copy has kernels for dstate 64 and 128, the NVFP4 copy for dstate 128.
 #define RSSM_FOR_EACH_CONFIG(X)                                                    \
   X(128, float, REPLAY_RC_NONE) X(128, float, REPLAY_RC_BF16) X(128, float, REPLAY_RC_FP8E4M3) \
   X(128, bf16, REPLAY_RC_NONE) X(128, bf16, REPLAY_RC_BF16) X(128, bf16, REPLAY_RC_FP8E4M3)   \
@@ -25,11 +25,13 @@ struct Shape {
   X(256, float, REPLAY_RC_NONE) X(256, float, REPLAY_RC_BF16) X(256, float, REPLAY_RC_FP8E4M3) \
   X(256, bf16, REPLAY_RC_NONE) X(256, bf16, REPLAY_RC_BF16) X(256, bf16, REPLAY_RC_FP8E4M3)   \
   X(128, float, REPLAY_RC_FP16) X(128, bf16, REPLAY_RC_FP16) X(64, float, REPLAY_RC_FP16)      \
-  X(64, bf16, REPLAY_RC_FP16)
+  X(64, bf16, REPLAY_RC_FP16) X(128, float, REPLAY_RC_NVFP4) X(128, bf16, REPLAY_RC_NVFP4)
 
 #define RSSM_DTYPE_OF(TT) (std::is_same<TT, float>::value ? REPLAY_F32 : REPLAY_BF16)
 
-int launch_step(const StoreView& sv, const Shape& sh, const void* x, const void* B, const void* C,
+// all_n: the ring count all sequences share before the step if the host knows it, else -1
+// (a kernel-choice hint only).
+int launch_step(const StoreView& sv, const Shape& sh, int all_n, const void* x, const void* B, const void* C,
                 const void* dt, float* y, cudaStream_t stream);
 int launch_verify(const StoreView& sv, const Shape& sh, int T, const void* x, const void* B,
                   const void* C, const void* dt, float* y, cudaStream_t stream);

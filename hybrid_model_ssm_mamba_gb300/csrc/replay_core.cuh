@@ -131,7 +131,7 @@ __device__ __forceinline__ void write_checkpoint(const StoreView& sv, size_t sla
                               static_cast<unsigned long long>(sv.batch) * sv.H, warp, lane, hv);
     else
       store_tile_rc<P, N, RC>(sv.rc, slab, 1.f, warp, lane, hv);
-  } else if constexpr (RC == REPLAY_RC_FP8E4M3) {
+  } else if constexpr (RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4) {
     float m = 0.f;
 #pragma unroll
     for (int i = 0; i < TL::RPW; ++i)
@@ -144,9 +144,39 @@ __device__ __forceinline__ void write_checkpoint(const StoreView& sv, size_t sla
     float amax = s_red[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, s_red[w]);
-    const float scale = amax > 0.f ? __fdiv_rn(amax, kE4M3Max) : 1.f;
-    if (tid == 0) sv.scale[slab] = scale;
-    store_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv);
+    if constexpr (RC == REPLAY_RC_FP8E4M3) {
+      const float scale = amax > 0.f ? __fdiv_rn(amax, kE4M3Max) : 1.f;
+      if (tid == 0) sv.scale[slab] = scale;
+      store_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv);
+    } else {
+      const float sg = amax > 0.f ? __fdiv_rn(amax, kE4M3Max * kE2M1Max) : 1.f;
+      if (tid == 0) sv.scale[slab] = sg;
+      store_tile_nvfp4<P, N>(sv.rc, sv.bscale, slab, sg, warp, lane, hv);
+    }
+  }
+}
+
+// The records' share of a non-flush output for the warp's RPW rows: record s (< k) sits on
+// lane s (and lane s + 32) and contributes c_s x_s[row]; each lane returns its partial per
+// row, to be summed over the warp.
+template <int RPW, class T, class XOf>
+__device__ __forceinline__ void record_terms(XOf x_of, const float* cf, int k, int warp, int lane,
+                                             float (&ex)[RPW]) {
+  if (lane < k) {
+    load_rows<RPW>(x_of(lane) + warp * RPW, ex);
+    const float c0 = cf[lane];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) ex[i] *= c0;
+  } else {
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) ex[i] = 0.f;
+  }
+  if (lane + 32 < k) {
+    float x1[RPW];
+    load_rows<RPW>(x_of(lane + 32) + warp * RPW, x1);
+    const float c1 = cf[lane + 32];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) ex[i] = fmaf(c1, x1[i], ex[i]);
   }
 }
 

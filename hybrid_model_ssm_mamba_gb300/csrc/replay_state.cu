@@ -29,8 +29,8 @@ replay_fold_kernel(StoreView sv, float* __restrict__ out) {
   if (tid == 0) s_meta = sv.meta[b];
   float hv[TL::RPW][TL::E];
   if (RC != REPLAY_RC_NONE && sv.shared) {  // the copy is the checkpoint
-    const float scale = RC == REPLAY_RC_FP8E4M3 ? sv.scale[slab] : 1.f;
-    load_tile_rc<P, N, RC == REPLAY_RC_NONE ? REPLAY_RC_BF16 : RC>(sv.rc, slab, scale, warp, lane, hv);
+    const float scale = RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4 ? sv.scale[slab] : 1.f;
+    load_tile_rc<P, N, RC == REPLAY_RC_NONE ? REPLAY_RC_BF16 : RC>(sv.rc, slab, scale, warp, lane, hv, sv.bscale);
   } else {
     load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
   }
@@ -127,6 +127,7 @@ int launch_load(const StoreView& sv, const Shape& sh, const float* h, const int*
   RSSM_LOAD(128, REPLAY_RC_NONE) RSSM_LOAD(128, REPLAY_RC_BF16) RSSM_LOAD(128, REPLAY_RC_FP8E4M3)
   RSSM_LOAD(256, REPLAY_RC_NONE) RSSM_LOAD(256, REPLAY_RC_BF16) RSSM_LOAD(256, REPLAY_RC_FP8E4M3)
   RSSM_LOAD(64, REPLAY_RC_FP16) RSSM_LOAD(128, REPLAY_RC_FP16)
+  RSSM_LOAD(128, REPLAY_RC_NVFP4)
 #undef RSSM_LOAD
   return REPLAY_EUNSUPPORTED;
 }

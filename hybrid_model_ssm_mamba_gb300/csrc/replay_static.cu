@@ -75,5 +75,7 @@ extern "C" int replay_step_static_scratch(replay_store* st, const void* x, const
   sv.arrive = reinterpret_cast<int*>(scratch);
   sv.plan = reinterpret_cast<int4*>(scratch + kArriveBytes);
   sv.coef = reinterpret_cast<float*>(scratch + kArriveBytes + kPlanBytes);
-  return rssm::launch_step(sv, st->sh, x, B, C, dt, y, s);
+  rc = rssm::launch_step(sv, st->sh, st->all_n, x, B, C, dt, y, s);
+  if (rc == REPLAY_OK) st->all_n = advance_all_n(st);
+  return rc;
 }

@@ -118,10 +118,13 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
   }
 }
 
+// expect_flush: the host knows every sequence flushes on this step, so a CTA with a read copy
+// loads the FP32 checkpoint (the flush's input) before the prep wait instead of the copy.
 template <int P, int N, class T, int RC>
 __global__ void __launch_bounds__(kThreads, kMinBlocks<N>)
 replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
-                   const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
+                   const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y,
+                   int expect_flush) {
   using TL = Tile<P, N>;
   constexpr int RPW = TL::RPW, E = TL::E;
   constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;  // 16-byte chunks per record
@@ -136,14 +139,19 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
   const size_t xo = static_cast<size_t>(slab) * P;  // x[b][h][:] and y[b][h][:]
   const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
 
-  // Independent of the prep kernel: the slab a non-flush step reads, C, x for D x.
+  // Independent of the prep kernel: the slab the step most likely reads, C, x for D x.
   float hv[RPW][E];
-  if constexpr (RC == REPLAY_RC_NONE) {
+  const bool f32_first = RC == REPLAY_RC_NONE || (expect_flush && !sv.shared);
+  auto load_copy = [&] {
+    if constexpr (RC != REPLAY_RC_NONE) {
+      const float scale = RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4 ? sv.scale[slab] : 1.f;
+      load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv, sv.bscale);
+    }
+  };
+  if (f32_first)
     load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
-  } else {
-    const float scale = RC == REPLAY_RC_FP8E4M3 ? sv.scale[slab] : 1.f;
-    load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv);
-  }
+  else
+    load_copy();
   float cv[E];
   load_cols<P, N>(C + bo, lane, cv);
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
@@ -163,23 +171,9 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
   auto x_of = [&](int s) { return s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P : x + xo; };
 
   if (pl.z == kPlanNonFlush) {
+    if (RC != REPLAY_RC_NONE && f32_first) load_copy();  // a non-flush step reads the copy
     float xr[RPW];
-    if (lane < k) {
-      load_rows<RPW>(x_of(lane) + warp * RPW, xr);
-      const float c0 = cf[lane];
-#pragma unroll
-      for (int i = 0; i < RPW; ++i) xr[i] *= c0;
-    } else {
-#pragma unroll
-      for (int i = 0; i < RPW; ++i) xr[i] = 0.f;
-    }
-    if (lane + 32 < k) {
-      float x1[RPW];
-      load_rows<RPW>(x_of(lane + 32) + warp * RPW, x1);
-      const float c1 = cf[lane + 32];
-#pragma unroll
-      for (int i = 0; i < RPW; ++i) xr[i] = fmaf(c1, x1[i], xr[i]);
-    }
+    record_terms<RPW, T>(x_of, cf, k, warp, lane, xr);
     const float sum = tile_rows_dot<P, N>(hv, cv, cf[cap], xr, lane);
     if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
     // append this token's record at ring slot start + n (B once per group, by its first head)
@@ -198,10 +192,8 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
   }
 
   // ---------------- flush: fold the k records into h0, write it once, read y from it
-  if constexpr (RC != REPLAY_RC_NONE) {  // a flush starts from the FP32 checkpoint
-    if (!sv.shared)                      // (a shared copy is the checkpoint: already loaded)
-      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
-  }
+  // (from the FP32 checkpoint; a shared copy is the checkpoint and is already loaded)
+  if (!f32_first && !sv.shared) load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
   float* sm_u = reinterpret_cast<float*>(smem4);  // [k][P]: w_s x_s
   float* sm_b = sm_u + cap * P;                   // [k][N]: B_s
   auto b_of = [&](int s) { return s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo; };
@@ -284,22 +276,7 @@ replay_step_copy_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
       const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
       auto x_of = [&](int s) { return s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P : x + xo; };
       float ex[RPW];
-      if (lane < k) {
-        load_rows<RPW>(x_of(lane) + warp * RPW, ex);
-        const float c0 = cf[lane];
-#pragma unroll
-        for (int i = 0; i < RPW; ++i) ex[i] *= c0;
-      } else {
-#pragma unroll
-        for (int i = 0; i < RPW; ++i) ex[i] = 0.f;
-      }
-      if (lane + 32 < k) {
-        float x1[RPW];
-        load_rows<RPW>(x_of(lane + 32) + warp * RPW, x1);
-        const float c1 = cf[lane + 32];
-#pragma unroll
-        for (int i = 0; i < RPW; ++i) ex[i] = fmaf(c1, x1[i], ex[i]);
-      }
+      record_terms<RPW, T>(x_of, cf, k, warp, lane, ex);
       const float gam = cf[cap];
       float part[RPW];
 #pragma unroll
@@ -369,6 +346,246 @@ replay_step_copy_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
 }
 
 // ---------------------------------------------------------------------------------------
+// NVFP4 copy (dstate 128). A slab's copy is 4 KiB of codes and 512 B of block scales, so a CTA
+// takes 8 heads of a group, one warp per head. h0 . C of a head is a 64 x 128 by 128 product,
+// done on the tensor cores with mma.sync m16n8k16 (f16 inputs, FP32 accumulation): one MMA
+// per (16-row tile, block), its k dimension one NVFP4 block, so the block scale applies to
+// its result. The codes become FP16 operands with integer ops only: slot A of a stored byte
+// is already the high byte of the FP16 value * 2^-14, slot B takes two shifts, and a byte
+// permute with zero places two codes in an FP16 pair. C enters as the B operand split into an
+// FP16 high and low part (columns 0 and 1; the other six columns are zero), after scaling the
+// group's C by a power of two that brings its largest value to [2^13, 2^14): the products are
+// exact in FP32 and C keeps about 22 bits. Lane (g, q) = (lane / 4, lane % 4) reads quarter q
+// of rows g and g + 8 of every 16-row tile (one 16-byte load each) and holds the A fragment
+// columns of that quarter; the MMA k index 2q, 2q+1, 2q+8, 2q+9 is block column 4q .. 4q+3.
+__device__ __forceinline__ void mma_16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                          unsigned b0, unsigned b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %10, %10, %10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+__device__ __forceinline__ unsigned prmt(unsigned a, unsigned b, unsigned sel) {
+  unsigned d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// The high FP16 bytes of the four slot-A codes, and of the four slot-B codes, of a word.
+__device__ __forceinline__ unsigned fp4_placed_a(unsigned w) { return w & 0x8E8E8E8Eu; }
+__device__ __forceinline__ unsigned fp4_placed_b(unsigned w) {
+  return ((w >> 3) & 0x0E0E0E0Eu) | ((w << 7) & 0x80808080u);
+}
+// FP16 pair (byte i, byte i + 1 of x as high bytes, zero low bytes)
+template <int I>
+__device__ __forceinline__ unsigned fp4_pair(unsigned x) {
+  return prmt(x, 0u, 4u | (I << 4) | (4u << 8) | ((I + 1) << 12));
+}
+// An E4M3 block scale as FP32: its 7 magnitude bits placed at bits 26..20 are the value times
+// 2^-120 (subnormal codes included, as FP32 denormals), so one exact multiply restores it.
+__device__ __forceinline__ float e4m3_scale_exact(unsigned code) {
+  return __int_as_float(static_cast<int>((code & 0x7fu) << 20)) * 0x1p120f;
+}
+
+// Dynamic shared memory of the NVFP4 kernel: per warp (head) its codes and block scales,
+// staged by cp.async before the prep wait, then its k records (x) staged after it.
+template <int P, int N, class T>
+constexpr size_t fp4_stage_bytes(int heads, int cap) {
+  return static_cast<size_t>(heads) * (P * N / 2 + P * N / kFp4Block) +
+         static_cast<size_t>(heads) * cap * P * sizeof(T);
+}
+
+template <int P, int N, class T, int HPC>
+__global__ void __launch_bounds__(kThreads, 3)
+replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
+                       const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
+  static_assert(P == 64 && N == 128 && HPC == kWarps && 2 * N == kThreads, "one warp per head, 64 x 128 slabs");
+  using TL = Tile<P, N>;
+  constexpr int RPW = TL::RPW, E = TL::E;
+  constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
+  constexpr int NB = N / kFp4Block, MT = P / 16;  // blocks per row, 16-row tiles
+  constexpr int CODE_BYTES = P * N / 2, SCALE_BYTES = P * NB;
+  extern __shared__ float4 smem4[];
+  __shared__ float s_red[kWarps];
+  __shared__ float s_y[kWarps][P];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, q = lane & 3;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int hfirst = g * sv.hpg + blockIdx.x * HPC;
+  const int slab0 = b * sv.H + hfirst;
+  const int cap = sv.cap;
+  const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
+  const int hw = hfirst + warp, slabw = slab0 + warp;  // this warp's head
+  const size_t xow = static_cast<size_t>(slabw) * P;
+
+  // Independent of the prep kernel: the head's codes and block scales into shared memory,
+  // C, x for D x.
+  uint8_t* s_codes = reinterpret_cast<uint8_t*>(smem4) + warp * (CODE_BYTES + SCALE_BYTES);
+  uint8_t* s_scales = s_codes + CODE_BYTES;
+  {
+    const uint8_t* codes = static_cast<const uint8_t*>(sv.rc) + static_cast<size_t>(slabw) * CODE_BYTES;
+    const uint8_t* scales = sv.bscale + static_cast<size_t>(slabw) * SCALE_BYTES;
+#pragma unroll
+    for (int c = lane; c < CODE_BYTES / 16; c += 32) cp_async16(s_codes + c * 16, codes + c * 16);
+#pragma unroll
+    for (int c = lane; c < SCALE_BYTES / 16; c += 32) cp_async16(s_scales + c * 16, scales + c * 16);
+    cp_async_commit();
+  }
+  // The group's C scaled by 2^sc and split into FP16 high and low parts, once per CTA (two
+  // threads per column), then each lane's B fragments (column gq: 0 = high, 1 = low, others
+  // zero).
+  __shared__ __half s_ch[2][N];
+  __shared__ float s_cmax[kWarps];
+  const int cc = tid & (N - 1);
+  const float cval = to_f(C[bo + cc]);
+  {
+    const float m = warp_max(fabsf(cval));
+    if (lane == 0) s_cmax[warp] = m;
+  }
+  __syncthreads();
+  float cmax = s_cmax[0];
+#pragma unroll
+  for (int w = 1; w < N / 32; ++w) cmax = fmaxf(cmax, s_cmax[w]);
+  const int ce = cmax > 0.f ? min(max(((__float_as_int(cmax) >> 23) & 0xff) - 127, -100), 100) : 0;
+  const float up = __int_as_float((127 + 13 - ce) << 23);    // 2^sc: largest |C| in [2^13, 2^14)
+  const float down = __int_as_float((127 + 1 + ce) << 23);   // 2^14 / 2^sc
+  {
+    const float cs = cval * up;
+    const __half hi = __float2half_rn(cs);
+    s_ch[tid / N][cc] = tid < N ? hi : __float2half_rn(cs - __half2float(hi));
+  }
+  __syncthreads();
+  unsigned bf[NB][2];
+#pragma unroll
+  for (int bk = 0; bk < NB; ++bk)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      bf[bk][j] = gq < 2 ? *reinterpret_cast<const unsigned*>(&s_ch[gq][bk * kFp4Block + 4 * q + 2 * j]) : 0u;
+  const float xk0 = to_f(x[xow + lane]), xk1 = to_f(x[xow + lane + 32]);
+
+  griddep_wait();  // plan and coefficients of this step are written
+  const int4 pl = sv.plan[b];
+  const int start = pl.x, n = pl.y;
+  if (pl.z == kPlanBad) {
+    if (tid < P)
+      for (int hh = 0; hh < HPC; ++hh) y[static_cast<size_t>(slab0 + hh) * P + tid] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const int k = n + 1;
+
+  if (pl.z == kPlanNonFlush) {
+    // Stage this head's k records (x) in shared memory by cp.async, and the coefficients in
+    // registers (lane s holds c_s and c_{s+32}); the MMAs below hide their latency.
+    const float* cf = sv.coef + static_cast<size_t>(slabw) * (cap + 1);
+    const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, hw, g);
+    T* sx = reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(smem4) + HPC * (CODE_BYTES + SCALE_BYTES)) +
+            static_cast<size_t>(warp) * cap * P;
+    for (int c = lane; c < k * XC; c += 32) {
+      const int s = c / XC, off = (c - s * XC) * EPC;
+      const T* src = s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P : x + xow;
+      cp_async16(sx + s * P + off, src + off);
+    }
+    cp_async_commit();
+    const float c_lo = lane < k ? cf[lane] : 0.f;
+    const float c_hi = lane + 32 < k ? cf[lane + 32] : 0.f;
+    const float gsc = cf[cap] * sv.scale[slabw] * down;
+    cp_async_wait_group<1>();  // the codes and scales (the records may still be in flight)
+    __syncwarp();
+    // h0 . C: rows gq and gq + 8 of each tile end up in the lanes with q == 0
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int r0 = mt * 16 + gq;
+      const uint4 W0 = *reinterpret_cast<const uint4*>(s_codes + fp4_unit(r0, 0, q));
+      const uint4 W1 = *reinterpret_cast<const uint4*>(s_codes + fp4_unit(r0 + 8, 0, q));
+      const uint2 S0 = *reinterpret_cast<const uint2*>(s_scales + r0 * NB);
+      const uint2 S1 = *reinterpret_cast<const uint2*>(s_scales + (r0 + 8) * NB);
+      float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) {  // word wd holds blocks 2 wd and 2 wd + 1
+        const unsigned w0 = wd == 0 ? W0.x : wd == 1 ? W0.y : wd == 2 ? W0.z : W0.w;
+        const unsigned w1 = wd == 0 ? W1.x : wd == 1 ? W1.y : wd == 2 ? W1.z : W1.w;
+        const unsigned a0 = fp4_placed_a(w0), b0 = fp4_placed_b(w0);
+        const unsigned a1 = fp4_placed_a(w1), b1 = fp4_placed_b(w1);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int bk = 2 * wd + half;
+          float d[4];
+          if (half == 0)
+            mma_16816(d, fp4_pair<0>(a0), fp4_pair<0>(a1), fp4_pair<0>(b0), fp4_pair<0>(b1), bf[bk][0], bf[bk][1]);
+          else
+            mma_16816(d, fp4_pair<2>(a0), fp4_pair<2>(a1), fp4_pair<2>(b0), fp4_pair<2>(b1), bf[bk][0], bf[bk][1]);
+          const unsigned s0 = bk < 4 ? S0.x >> (8 * bk) : S0.y >> (8 * (bk - 4));
+          const unsigned s1 = bk < 4 ? S1.x >> (8 * bk) : S1.y >> (8 * (bk - 4));
+          y0 = fmaf(e4m3_scale_exact(s0), d[0] + d[1], y0);
+          y1 = fmaf(e4m3_scale_exact(s1), d[2] + d[3], y1);
+        }
+      }
+      if (q == 0) {
+        s_y[warp][mt * 16 + gq] = y0;
+        s_y[warp][mt * 16 + gq + 8] = y1;
+      }
+    }
+    cp_async_wait_all();
+    __syncwarp();
+    // records: lane holds rows lane and lane + 32
+    float ex0 = 0.f, ex1 = 0.f;
+    for (int s = 0; s < k; ++s) {
+      const float c = __shfl_sync(kFull, s < 32 ? c_lo : c_hi, s & 31);
+      ex0 = fmaf(c, to_f(sx[s * P + lane]), ex0);
+      ex1 = fmaf(c, to_f(sx[s * P + lane + 32]), ex1);
+    }
+    const float Dh = sv.D[hw];
+    y[xow + lane] = fmaf(Dh, xk0, fmaf(gsc, s_y[warp][lane], ex0));
+    y[xow + lane + 32] = fmaf(Dh, xk1, fmaf(gsc, s_y[warp][lane + 32], ex1));
+    // append this head's record at ring slot start + n (B once per group: warp 0 of the
+    // group's first CTA)
+    const int slot = ring_slot(start, n, cap);
+    if (lane < XC)
+      *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + lane * EPC) =
+          *reinterpret_cast<const uint4*>(x + xow + lane * EPC);
+    if (lane == 31) ring.dt[slot] = dt[slabw];
+    if (blockIdx.x == 0 && warp == 0)
+      for (int c = lane; c < BC; c += 32)
+        *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+            *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+    return;
+  }
+
+  // ---------------- flush, head by head, the whole CTA on each
+  cp_async_wait_all();  // the staged codes share the shared memory the fold stages into
+  __syncthreads();
+  float cv[E];
+  load_cols<P, N>(C + bo, lane, cv);
+  const int myrow = warp * RPW + transpose_index<RPW>(lane);
+  float* sm_u = reinterpret_cast<float*>(smem4);
+  float* sm_b = sm_u + cap * P;
+  for (int hh = 0; hh < HPC; ++hh) {
+    const int h = hfirst + hh, slab = slab0 + hh;
+    const size_t xo = static_cast<size_t>(slab) * P;
+    const float* cf = sv.coef + static_cast<size_t>(slab) * (cap + 1);
+    const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+    float hv[RPW][E];
+    if (sv.shared)
+      load_tile_rc<P, N, REPLAY_RC_NVFP4>(sv.rc, slab, sv.scale[slab], warp, lane, hv, sv.bscale);
+    else
+      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    auto x_of = [&](int s) { return s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P : x + xo; };
+    auto b_of = [&](int s) { return s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo; };
+    if (hh > 0) __syncthreads();  // the previous head's staging has been read
+    stage_weighted<P, N, T>(x_of, b_of, cf, k, sm_u, sm_b);
+    __syncthreads();
+    fold_staged<P, N>(sm_u, sm_b, k, cf[cap], hv);
+    float zero[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) zero[i] = 0.f;
+    const float sum = tile_rows_dot<P, N>(hv, cv, 1.f, zero, lane);
+    if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
+    write_checkpoint<P, N, REPLAY_RC_NVFP4>(sv, slab, s_red, hv, pl.w);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // Small calls (few slabs, so few waves): one fused kernel. Each head's CTA copies its slab's
 // whole ring (x of the head, B of the group, dt) and the current record into a shared-memory
 // image with cp.async while its checkpoint loads are in flight -- nothing waits on the ring
@@ -406,8 +623,8 @@ replay_step_fused_kernel(StoreView sv, const T* __restrict__ x, const T* __restr
   if constexpr (RC == REPLAY_RC_NONE) {
     load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
   } else {
-    const float scale = RC == REPLAY_RC_FP8E4M3 ? sv.scale[slab] : 1.f;
-    load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv);
+    const float scale = RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4 ? sv.scale[slab] : 1.f;
+    load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv, sv.bscale);
   }
   const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
   RingImage<T> im;
@@ -500,46 +717,15 @@ replay_step_fused_kernel(StoreView sv, const T* __restrict__ x, const T* __restr
 // Calls with at most this many (sequence, head) slabs take the fused kernel.
 constexpr long long kFusedMaxSlabs = 1024;
 
-template <int P, int N, class T, int RC>
-static int launch(const StoreView& sv, const void* x, const void* B, const void* C, const void* dt,
-                  float* y, cudaStream_t stream) {
-  if (static_cast<long long>(sv.batch) * sv.H <= kFusedMaxSlabs) {
-    auto fused = replay_step_fused_kernel<P, N, T, RC>;
-    const size_t fsmem = smem_plan_bytes<P, N>(whole_image_bytes<P, N, T>(sv.cap), sv.cap);
-    if (fsmem > 48 * 1024 &&
-        cudaFuncSetAttribute(fused, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(fsmem)) !=
-            cudaSuccess)
-      return REPLAY_ECUDA;
-    fused<<<dim3(sv.hpg, sv.G, sv.batch), kThreads, fsmem, stream>>>(
-        sv, static_cast<const T*>(x), static_cast<const T*>(B), static_cast<const T*>(C),
-        static_cast<const T*>(dt), y);
-    return cudaGetLastError() == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA;
-  }
-  auto prep = replay_step_prep_kernel<P, N, T>;
-  const size_t psmem = static_cast<size_t>(sv.cap + 1) * N * sizeof(T);
-  if (psmem > 48 * 1024 &&
-      cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
-          cudaSuccess)
-    return REPLAY_ECUDA;
-  prep<<<dim3(sv.G, sv.batch), kPrepThreads, psmem, stream>>>(sv, static_cast<const T*>(B), static_cast<const T*>(C),
-                                                          static_cast<const T*>(dt));
-  if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
-  auto kern = replay_step_kernel<P, N, T, RC>;
-  int heads = 1;  // heads per CTA
-  if constexpr (RC != REPLAY_RC_NONE) {
-    constexpr int HPC = heads_per_cta<N, RC>();
-    if (HPC > 1 && sv.hpg % HPC == 0) {
-      kern = replay_step_copy_kernel<P, N, T, RC, HPC>;
-      heads = HPC;
-    }
-  }
-  const size_t smem = fold_staging_bytes<P, N>(sv.cap);
+// Launch a per-head kernel as a programmatic dependent of the prep kernel before it.
+template <class... KArgs, class... Args>
+static int pdl_launch(void (*kern)(KArgs...), dim3 grid, size_t smem, cudaStream_t stream, Args... args) {
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sv.hpg / heads, sv.G, sv.batch);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -548,16 +734,61 @@ static int launch(const StoreView& sv, const void* x, const void* B, const void*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, sv, static_cast<const T*>(x), static_cast<const T*>(B),
-                                           static_cast<const T*>(C), static_cast<const T*>(dt), y);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA;
 }
 
-int launch_step(const StoreView& sv, const Shape& sh, const void* x, const void* B, const void* C,
+// all_n: the ring count every sequence holds before this step when the host knows it (-1
+// otherwise). It only picks kernels: every kernel handles any mix of flush and non-flush
+// sequences. A step the host knows flushes every sequence takes the one-head-per-CTA kernel
+// (more slabs in flight for the FP32 read and write); otherwise a read copy takes the
+// several-heads-per-CTA kernels built for the small copy reads.
+template <int P, int N, class T, int RC>
+static int launch(const StoreView& sv, int all_n, const void* x, const void* B, const void* C, const void* dt,
+                  float* y, cudaStream_t stream) {
+  const T *tx = static_cast<const T*>(x), *tB = static_cast<const T*>(B), *tC = static_cast<const T*>(C),
+          *tdt = static_cast<const T*>(dt);
+  if (static_cast<long long>(sv.batch) * sv.H <= kFusedMaxSlabs) {
+    auto fused = replay_step_fused_kernel<P, N, T, RC>;
+    const size_t fsmem = smem_plan_bytes<P, N>(whole_image_bytes<P, N, T>(sv.cap), sv.cap);
+    if (fsmem > 48 * 1024 &&
+        cudaFuncSetAttribute(fused, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(fsmem)) !=
+            cudaSuccess)
+      return REPLAY_ECUDA;
+    fused<<<dim3(sv.hpg, sv.G, sv.batch), kThreads, fsmem, stream>>>(sv, tx, tB, tC, tdt, y);
+    return cudaGetLastError() == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA;
+  }
+  auto prep = replay_step_prep_kernel<P, N, T>;
+  const size_t psmem = static_cast<size_t>(sv.cap + 1) * N * sizeof(T);
+  if (psmem > 48 * 1024 &&
+      cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
+          cudaSuccess)
+    return REPLAY_ECUDA;
+  prep<<<dim3(sv.G, sv.batch), kPrepThreads, psmem, stream>>>(sv, tB, tC, tdt);
+  if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
+  const size_t smem = fold_staging_bytes<P, N>(sv.cap);
+  const bool all_flush = all_n >= 0 && all_n + 1 >= sv.L;
+  if constexpr (RC == REPLAY_RC_NVFP4 && N == 128) {
+    constexpr int HPC = 8;
+    const size_t fsmem = std::max(smem, fp4_stage_bytes<P, N, T>(HPC, sv.cap));
+    if (!all_flush && sv.hpg % HPC == 0)
+      return pdl_launch(replay_step_fp4_kernel<P, N, T, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch), fsmem, stream,
+                        sv, tx, tB, tC, tdt, y);
+  } else if constexpr (RC != REPLAY_RC_NONE && RC != REPLAY_RC_NVFP4) {
+    constexpr int HPC = heads_per_cta<N, RC>();
+    if (!all_flush && HPC > 1 && sv.hpg % HPC == 0)
+      return pdl_launch(replay_step_copy_kernel<P, N, T, RC, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch), smem,
+                        stream, sv, tx, tB, tC, tdt, y);
+  }
+  return pdl_launch(replay_step_kernel<P, N, T, RC>, dim3(sv.hpg, sv.G, sv.batch), smem, stream, sv, tx, tB, tC,
+                    tdt, y, all_flush ? 1 : 0);
+}
+
+int launch_step(const StoreView& sv, const Shape& sh, int all_n, const void* x, const void* B, const void* C,
                 const void* dt, float* y, cudaStream_t stream) {
 #define RSSM_STEP(NN, TT, RCC)                                                  \
   if (sh.N == NN && sh.in_dtype == RSSM_DTYPE_OF(TT) && sh.read_copy == RCC)    \
-    return launch<64, NN, TT, RCC>(sv, x, B, C, dt, y, stream);
+    return launch<64, NN, TT, RCC>(sv, all_n, x, B, C, dt, y, stream);
   RSSM_FOR_EACH_CONFIG(RSSM_STEP)
 #undef RSSM_STEP
   return REPLAY_EUNSUPPORTED;

@@ -29,12 +29,16 @@ namespace rssm {
 constexpr int kMaxDrafts = 8;
 constexpr int kVerifyBad = -1, kVerifyPlain = 0, kVerifyPrefold = 1;
 
-constexpr int kPrepThreads = 128, kPrepWarps = kPrepThreads / 32;  // small: see the step's prep
+// The prep's CTA size: 256 threads when the whole prep grid fits on the GPU at once with room
+// to spare (its serial per-head work then spreads over 8 warps), else 128 so that every prep
+// CTA is resident before the dependent per-head kernel needs them (as for the step's prep).
+constexpr long long kPrepWideMaxThreads = 152LL * 1024;
 
-template <int P, int N, class T>
+template <int P, int N, class T, int kPrepThreads>
 __global__ void __launch_bounds__(kPrepThreads)
 replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T* __restrict__ C,
                           const T* __restrict__ dt) {
+  constexpr int kPrepWarps = kPrepThreads / 32;
   using TL = Tile<P, N>;
   __shared__ int4 s_meta;
   __shared__ float s_bc[kMaxDrafts][kMaxCap];
@@ -153,8 +157,8 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
   if constexpr (RC == REPLAY_RC_NONE) {
     load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
   } else {
-    const float scale = RC == REPLAY_RC_FP8E4M3 ? sv.scale[slab] : 1.f;
-    load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv);
+    const float scale = RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4 ? sv.scale[slab] : 1.f;
+    load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv, sv.bscale);
   }
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
   const float Dh = sv.D[h];
@@ -244,14 +248,15 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
 template <int P, int N, class T, int RC>
 static int launch(const StoreView& sv, int TT, const void* x, const void* B, const void* C,
                   const void* dt, float* y, cudaStream_t stream) {
-  auto prep = replay_verify_prep_kernel<P, N, T>;
+  const bool wide = static_cast<long long>(sv.G) * sv.batch * 256 <= kPrepWideMaxThreads;
+  auto prep = wide ? replay_verify_prep_kernel<P, N, T, 256> : replay_verify_prep_kernel<P, N, T, 128>;
   const size_t psmem = static_cast<size_t>(sv.cap + kMaxDrafts) * N * sizeof(T);
   if (psmem > 48 * 1024 &&
       cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
-  prep<<<dim3(sv.G, sv.batch), kPrepThreads, psmem, stream>>>(sv, TT, static_cast<const T*>(B),
-                                                          static_cast<const T*>(C), static_cast<const T*>(dt));
+  prep<<<dim3(sv.G, sv.batch), wide ? 256 : 128, psmem, stream>>>(sv, TT, static_cast<const T*>(B),
+                                                              static_cast<const T*>(C), static_cast<const T*>(dt));
   if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
   auto kern = replay_verify_kernel<P, N, T, RC>;
   const size_t smem = fold_staging_bytes<P, N>(sv.cap) + static_cast<size_t>(TT) * (P + N) * sizeof(T);

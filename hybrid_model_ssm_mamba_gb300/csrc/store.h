@@ -9,4 +9,13 @@ struct replay_store {
   char* ws;
   rssm::StoreView sv;
   rssm::Shape sh;
+  // The ring count every sequence holds, while the host can know it: 0 after an alloc, a
+  // full reset, a load or a flush, advanced by each step; -1 (unknown) after a masked reset,
+  // a verify or a commit, whose effect depends on device data. Picks kernels only.
+  int all_n;
 };
+
+// The step's hint, and the count after a step launched with it.
+inline int advance_all_n(const replay_store* st) {
+  return st->all_n < 0 ? -1 : (st->all_n + 1 >= st->cfg.window_L ? 0 : st->all_n + 1);
+}

@@ -20,6 +20,7 @@ from . import build as _build
 __all__ = [
     "ReplayError", "ReplayConfig", "ReplayLayout", "load_library", "header_functions",
     "REPLAY_F32", "REPLAY_BF16", "REPLAY_RC_NONE", "REPLAY_RC_BF16", "REPLAY_RC_FP8E4M3", "REPLAY_RC_FP16",
+    "REPLAY_RC_NVFP4",
     "REPLAY_DEV_BAD_META", "REPLAY_DEV_BAD_ACCEPT",
     "replay_layout_of", "replay_store_bytes", "replay_alloc", "replay_free", "replay_reset",
     "replay_load_state", "replay_export_state", "replay_step", "replay_verify",
@@ -30,7 +31,7 @@ __all__ = [
 HEADER = pathlib.Path(__file__).resolve().parent.parent / "include" / "replayssm.h"
 
 REPLAY_F32, REPLAY_BF16 = 0, 1
-REPLAY_RC_NONE, REPLAY_RC_BF16, REPLAY_RC_FP8E4M3, REPLAY_RC_FP16 = 0, 1, 2, 3
+REPLAY_RC_NONE, REPLAY_RC_BF16, REPLAY_RC_FP8E4M3, REPLAY_RC_FP16, REPLAY_RC_NVFP4 = 0, 1, 2, 3, 4
 REPLAY_DEV_BAD_META, REPLAY_DEV_BAD_ACCEPT = 1, 2
 REPLAY_STATIC_MAX_BATCH = 4096
 REPLAY_STATIC_MAX_COEFS = 1048576
@@ -60,7 +61,7 @@ class ReplayConfig(ctypes.Structure):
 
 class ReplayLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "h0", "rc", "scale", "xbuf", "bbuf", "dtbuf", "meta", "arrive", "status", "plan", "coef",
+        "h0", "rc", "scale", "bscale", "xbuf", "bbuf", "dtbuf", "meta", "arrive", "status", "plan", "coef",
         "total")] + \
         [("cap", ctypes.c_int)]
 
@@ -292,8 +293,11 @@ class ReplayStore:
             "h0": (torch.float32, (0,) if c.shared_checkpoint else (Bz, H, P, N)),
             "rc": ({REPLAY_RC_BF16: torch.bfloat16, REPLAY_RC_FP8E4M3: torch.uint8,
                     REPLAY_RC_FP16: torch.float16}.get(c.read_copy, torch.uint8),
+                   (Bz, H, P, N // 2) if c.read_copy == REPLAY_RC_NVFP4 else
                    (Bz, H, P, N) if c.read_copy else (0,)),
-            "scale": (torch.float32, (Bz, H) if c.read_copy == REPLAY_RC_FP8E4M3 else (0,)),
+            "scale": (torch.float32,
+                      (Bz, H) if c.read_copy in (REPLAY_RC_FP8E4M3, REPLAY_RC_NVFP4) else (0,)),
+            "bscale": (torch.uint8, (Bz, H, P, N // 16) if c.read_copy == REPLAY_RC_NVFP4 else (0,)),
             "xbuf": (dt, (Bz, H, cap, P)), "bbuf": (dt, (Bz, G, cap, N)), "dtbuf": (dt, (Bz, H, cap)),
             "meta": (torch.int32, (Bz, 4)), "arrive": (torch.int32, (Bz,)), "status": (torch.int32, (1,)),
             "plan": (torch.int32, (Bz, 4)),

@@ -67,6 +67,19 @@ extern "C" {
                               * give u, and the value rounds away from zero iff u is below its
                               * distance from the lower neighbour over the neighbours' spacing.
                               * dstate 64 and 128 only. */
+#define REPLAY_RC_NVFP4 4    /* NVFP4: E2M1 codes, one E4M3 scale per 16 consecutive elements of
+                              * a row, one FP32 scale per (b, h) slab: s_g = absmax / 2688 (1 if
+                              * the slab is zero); s_b = e4m3(block_absmax / (6 s_g)); e = s_b s_g;
+                              * q = e2m1(h / e) (RNE, saturating at 6; 0 where e = 0), each step
+                              * one FP32 operation. The post's sections "Benefit 3" and "State
+                              * quantization" read this format. dstate 128 only. Code layout of
+                              * a row (64 bytes): quarter u (0..3) of block b (columns 16b+4u ..
+                              * 16b+4u+3) is the 2-byte unit at byte 16u + 2b; the unit's byte 0
+                              * holds columns 16b+4u (slot A) and 16b+4u+2 (slot B), byte 1
+                              * columns 16b+4u+1 (A) and 16b+4u+3 (B); slot A keeps the code's
+                              * sign in bit 7 and magnitude in bits 3..1, slot B the sign in bit
+                              * 0 and magnitude in bits 6..4 (E2M1 code = sign * 8 + magnitude).
+                              * Block scales are [P][N/16] row-major. */
 
 /* host return codes */
 #define REPLAY_OK 0
@@ -99,7 +112,9 @@ typedef struct replay_config {
 /* Byte offsets of the regions inside the caller's workspace (each 256-byte aligned).
  *   h0     FP32 checkpoint            [batch][H][P][N]
  *   rc     read copy (bf16/E4M3/FP16) [batch][H][P][N]      (0 bytes without a copy)
- *   scale  FP32 E4M3 scale            [batch][H]            (0 bytes unless E4M3)
+ *          NVFP4 codes                [batch][H][P][N/2] bytes (row layout: REPLAY_RC_NVFP4)
+ *   scale  FP32 slab scale            [batch][H]            (E4M3 and NVFP4 only)
+ *   bscale NVFP4 E4M3 block scales    [batch][H][P][N/16]   (NVFP4 only)
  *   xbuf   ring of x records          [batch][H][cap][P]    (in_dtype)
  *   bbuf   ring of B records          [batch][G][cap][N]    (in_dtype)
  *   dtbuf  ring of dt records         [batch][H][cap]       (in_dtype)
@@ -116,7 +131,7 @@ typedef struct replay_config {
  * records a sequence can hold (window_L - 1 + T committed before a verify folds them)
  * plus T drafts written beyond them while those are being folded. */
 typedef struct replay_layout {
-  size_t h0, rc, scale, xbuf, bbuf, dtbuf, meta, arrive, status, plan, coef;
+  size_t h0, rc, scale, bscale, xbuf, bbuf, dtbuf, meta, arrive, status, plan, coef;
   size_t total;  /* workspace bytes */
   int cap;       /* ring capacity in records */
 } replay_layout;

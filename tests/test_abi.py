@@ -40,8 +40,19 @@ def test_layout_ring_capacity_and_read_copies():
         assert L.scale - L.rc == 512 * 8 * 64 * 128 * 2 and L.xbuf == L.scale
 
 
-def test_fp16_copy_has_no_dstate_256_kernel():
-    cfg = R.ReplayConfig(4, 8, 64, 256, 4, 16, 0, R.REPLAY_F32, R.REPLAY_RC_FP16, 1)
+def test_layout_nvfp4_regions():
+    cfg = R.ReplayConfig(512, 8, 64, 128, 1, 16, 0, R.REPLAY_F32, R.REPLAY_RC_NVFP4)
+    L = R.replay_layout_of(cfg)
+    assert L.scale - L.rc == 512 * 8 * 64 * 128 // 2        # two codes per byte
+    assert L.bscale - L.scale == 512 * 8 * 4                 # FP32 slab scale
+    assert L.xbuf - L.bscale == 512 * 8 * 64 * 128 // 16     # one E4M3 scale per 16 values
+    assert R.replay_store_bytes(cfg) == L.total
+
+
+@pytest.mark.parametrize("rc,dstate", [(R.REPLAY_RC_FP16, 256), (R.REPLAY_RC_NVFP4, 256),
+                                       (R.REPLAY_RC_NVFP4, 64)])
+def test_copies_without_a_kernel_for_the_dstate(rc, dstate):
+    cfg = R.ReplayConfig(4, 8, 64, dstate, 4, 16, 0, R.REPLAY_F32, rc, 1)
     with pytest.raises(R.ReplayError) as e:
         R.replay_layout_of(cfg)
     assert e.value.code == -2
@@ -49,7 +60,7 @@ def test_fp16_copy_has_no_dstate_256_kernel():
 
 @pytest.mark.parametrize("field,value,code", [
     ("batch", 0, -1), ("nheads", 6, -1), ("ngroups", 0, -1), ("window_L", 0, -1),
-    ("max_draft_T", -1, -1), ("in_dtype", 7, -1), ("read_copy", 4, -1), ("headdim", 48, -2),
+    ("max_draft_T", -1, -1), ("in_dtype", 7, -1), ("read_copy", 5, -1), ("headdim", 48, -2),
     ("dstate", 96, -2), ("window_L", 65, -3), ("max_draft_T", 9, -3)])
 def test_layout_rejects(field, value, code):
     cfg = R.ReplayConfig(4, 8, 64, 128, 4, 16, 2, R.REPLAY_F32, R.REPLAY_RC_NONE)

@@ -12,6 +12,7 @@ from gpu_util import DTYPE, draft_device, make_store, rel_vec_err, step_inputs
 from hybrid_model_ssm_mamba_gb300 import replay as R
 from oracle import formats as F
 from oracle.mamba2 import Mamba2Decoder
+from test_gpu_nvfp4 import device_codes
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
@@ -354,7 +355,7 @@ class _SrRounder:
 
 
 @pytest.mark.parametrize("rc,tol", [(R.REPLAY_RC_BF16, 5e-3), (R.REPLAY_RC_FP8E4M3, 5e-2),
-                                    (R.REPLAY_RC_FP16, 1e-3)])
+                                    (R.REPLAY_RC_FP16, 1e-3), (R.REPLAY_RC_NVFP4, 5e-2)])
 @pytest.mark.parametrize("batch,heads,groups", [(4, 8, 2), (72, 128, 8)])
 def test_shared_checkpoint_matches_periodic_rounding(rc, tol, batch, heads, groups):
     """With shared_checkpoint the low-precision copy is the recurrence state: every flush
@@ -369,7 +370,7 @@ def test_shared_checkpoint_matches_periodic_rounding(rc, tol, batch, heads, grou
     st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
     sel = np.array([0, batch - 1])
     rounder = {R.REPLAY_RC_BF16: F.bf16_round_state, R.REPLAY_RC_FP8E4M3: F.e4m3_round_state,
-               R.REPLAY_RC_FP16: _SrRounder(sel, batch * heads)}[rc]
+               R.REPLAY_RC_FP16: _SrRounder(sel, batch * heads), R.REPLAY_RC_NVFP4: F.nvfp4_round_state}[rc]
     z = np.zeros((2, heads, 64, 128))
     rounded = Mamba2Decoder(A.astype(float), D.astype(float), groups, z, window_round=rounder, window_L=L)
     plain = Mamba2Decoder(A.astype(float), D.astype(float), groups, z)
@@ -389,13 +390,21 @@ def test_shared_checkpoint_matches_periodic_rounding(rc, tol, batch, heads, grou
         assert not np.any(hg.view(np.uint32) & 0xFFFF)
     elif rc == R.REPLAY_RC_FP16:
         assert np.array_equal(hg, hg.astype(np.float16).astype(np.float32))
+    elif rc == R.REPLAY_RC_NVFP4:
+        q = device_codes(st.region("rc").cpu().numpy())
+        sb, sgl = st.region("bscale").cpu().numpy(), st.region("scale").cpu().numpy()
+        for i in sel:
+            for hh in range(heads):
+                back = F.nvfp4_slab_dequantize(q[i, hh], sb[i, hh], sgl[i, hh]).astype(np.float32)
+                assert np.array_equal(back, hg[i, hh]), (i, hh)
     else:
         scale = st.region("scale").cpu().numpy()[:, :, None, None]
         assert np.array_equal(F.fp8_slab_dequantize(F.e4m3_encode(hg / scale), scale), hg)
     # ... and follows the rounded oracle. FP32 and FP64 states can round a value that sits
     # near a midpoint (or a scale) differently: such flips move one element by one code
     # step and are rare; everything else agrees to FP32 accuracy.
-    step = {R.REPLAY_RC_BF16: 2.0 ** -7, R.REPLAY_RC_FP8E4M3: 32 / 448, R.REPLAY_RC_FP16: 2.0 ** -10}[rc]
+    step = {R.REPLAY_RC_BF16: 2.0 ** -7, R.REPLAY_RC_FP8E4M3: 32 / 448, R.REPLAY_RC_FP16: 2.0 ** -10,
+            R.REPLAY_RC_NVFP4: 1 / 3}[rc]
     d = np.abs(hg[sel] - rounded.h) / np.abs(rounded.h).max(axis=(2, 3), keepdims=True)
     assert d.max() <= 2 * step and (d > 1e-5).mean() <= 1e-3, (d.max(), (d > 1e-5).mean())
     assert e_round <= tol and e_plain > 2 * e_round, (e_round, e_plain)
