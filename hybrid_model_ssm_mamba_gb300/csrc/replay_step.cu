@@ -358,13 +358,14 @@ replay_step_copy_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
 // exact in FP32 and C keeps about 22 bits. Lane (g, q) = (lane / 4, lane % 4) reads quarter q
 // of rows g and g + 8 of every 16-row tile (one 16-byte load each) and holds the A fragment
 // columns of that quarter; the MMA k index 2q, 2q+1, 2q+8, 2q+9 is block column 4q .. 4q+3.
+// d += a b
 __device__ __forceinline__ void mma_16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
                                           unsigned b0, unsigned b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%10, %10, %10, %10};\n"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+      "{%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ unsigned prmt(unsigned a, unsigned b, unsigned sel) {
   unsigned d;
@@ -381,10 +382,19 @@ template <int I>
 __device__ __forceinline__ unsigned fp4_pair(unsigned x) {
   return prmt(x, 0u, 4u | (I << 4) | (4u << 8) | ((I + 1) << 12));
 }
-// An E4M3 block scale as FP32: its 7 magnitude bits placed at bits 26..20 are the value times
-// 2^-120 (subnormal codes included, as FP32 denormals), so one exact multiply restores it.
-__device__ __forceinline__ float e4m3_scale_exact(unsigned code) {
-  return __int_as_float(static_cast<int>((code & 0x7fu) << 20)) * 0x1p120f;
+// Two E4M3 block scales (bytes I and I + 1 of w) as an FP16 pair: a code's 7 magnitude bits
+// placed at bits 13..7 of an FP16 are its value times 2^-8 (subnormal codes included, as FP16
+// subnormals), so one exact multiply by 256 restores it.
+template <int I>
+__device__ __forceinline__ __half2 fp16_scale_pair(unsigned w) {
+  const unsigned t = (prmt(w, 0u, I | (4u << 4) | ((I + 1) << 8) | (4u << 12)) << 7) & 0x3F803F80u;
+  return __hmul2(*reinterpret_cast<const __half2*>(&t), __float2half2_rn(256.f));
+}
+// An FP16 pair times one FP16 scale (exact here: a code times a scale has at most 6
+// significant bits and stays a multiple of 2^-24 below 1).
+__device__ __forceinline__ unsigned scale_pair(unsigned p, __half s) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&p), __half2half2(s));
+  return *reinterpret_cast<const unsigned*>(&r);
 }
 
 // Dynamic shared memory of the NVFP4 kernel: per warp (head) its codes and block scales,
@@ -500,30 +510,33 @@ replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restric
       const uint4 W1 = *reinterpret_cast<const uint4*>(s_codes + fp4_unit(r0 + 8, 0, q));
       const uint2 S0 = *reinterpret_cast<const uint2*>(s_scales + r0 * NB);
       const uint2 S1 = *reinterpret_cast<const uint2*>(s_scales + (r0 + 8) * NB);
-      float y0 = 0.f, y1 = 0.f;
+      // The A operands carry their block scale (the MMAs then accumulate over the blocks).
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int wd = 0; wd < 4; ++wd) {  // word wd holds blocks 2 wd and 2 wd + 1
         const unsigned w0 = wd == 0 ? W0.x : wd == 1 ? W0.y : wd == 2 ? W0.z : W0.w;
         const unsigned w1 = wd == 0 ? W1.x : wd == 1 ? W1.y : wd == 2 ? W1.z : W1.w;
+        const unsigned sw0 = wd < 2 ? S0.x : S0.y, sw1 = wd < 2 ? S1.x : S1.y;
+        const __half2 sc0 = (wd & 1) ? fp16_scale_pair<2>(sw0) : fp16_scale_pair<0>(sw0);  // row gq
+        const __half2 sc1 = (wd & 1) ? fp16_scale_pair<2>(sw1) : fp16_scale_pair<0>(sw1);  // row gq + 8
         const unsigned a0 = fp4_placed_a(w0), b0 = fp4_placed_b(w0);
         const unsigned a1 = fp4_placed_a(w1), b1 = fp4_placed_b(w1);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int bk = 2 * wd + half;
-          float d[4];
-          if (half == 0)
-            mma_16816(d, fp4_pair<0>(a0), fp4_pair<0>(a1), fp4_pair<0>(b0), fp4_pair<0>(b1), bf[bk][0], bf[bk][1]);
-          else
-            mma_16816(d, fp4_pair<2>(a0), fp4_pair<2>(a1), fp4_pair<2>(b0), fp4_pair<2>(b1), bf[bk][0], bf[bk][1]);
-          const unsigned s0 = bk < 4 ? S0.x >> (8 * bk) : S0.y >> (8 * (bk - 4));
-          const unsigned s1 = bk < 4 ? S1.x >> (8 * bk) : S1.y >> (8 * (bk - 4));
-          y0 = fmaf(e4m3_scale_exact(s0), d[0] + d[1], y0);
-          y1 = fmaf(e4m3_scale_exact(s1), d[2] + d[3], y1);
+        {
+          const int bk = 2 * wd;
+          const __half s0 = __low2half(sc0), s1 = __low2half(sc1);
+          mma_16816(acc, scale_pair(fp4_pair<0>(a0), s0), scale_pair(fp4_pair<0>(a1), s1),
+                    scale_pair(fp4_pair<0>(b0), s0), scale_pair(fp4_pair<0>(b1), s1), bf[bk][0], bf[bk][1]);
+        }
+        {
+          const int bk = 2 * wd + 1;
+          const __half s0 = __high2half(sc0), s1 = __high2half(sc1);
+          mma_16816(acc, scale_pair(fp4_pair<2>(a0), s0), scale_pair(fp4_pair<2>(a1), s1),
+                    scale_pair(fp4_pair<2>(b0), s0), scale_pair(fp4_pair<2>(b1), s1), bf[bk][0], bf[bk][1]);
         }
       }
       if (q == 0) {
-        s_y[warp][mt * 16 + gq] = y0;
-        s_y[warp][mt * 16 + gq + 8] = y1;
+        s_y[warp][mt * 16 + gq] = acc[0] + acc[1];
+        s_y[warp][mt * 16 + gq + 8] = acc[2] + acc[3];
       }
     }
     cp_async_wait_all();

@@ -211,14 +211,18 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
   auto x_of = [&](int s) {
     return s < n2 ? ring.x + static_cast<size_t>(ring_slot(start2, s, cap)) * P : x + xoff(s - n2);
   };
+  // the drafts' coefficients to shared memory in one round trip (not one per draft)
+  float* s_cf = reinterpret_cast<float*>(sx + static_cast<size_t>(TT) * P);
+  for (int i = tid; i < TT * cs; i += kThreads) s_cf[i] = cf[cs + i];
   float xr0[RPW], xr1[RPW];  // records lane and lane + 32: x values of this warp's rows
 #pragma unroll
   for (int i = 0; i < RPW; ++i) xr0[i] = xr1[i] = 0.f;
   if (lane < kk) load_rows<RPW>(x_of(lane) + warp * RPW, xr0);
   if (lane + 32 < kk) load_rows<RPW>(x_of(lane + 32) + warp * RPW, xr1);
+  __syncthreads();
   for (int j = 0; j < TT; ++j) {
     const int k = n2 + j + 1;  // records draft j sees, itself included
-    const float* cj = cf + (1 + j) * cs;
+    const float* cj = s_cf + j * cs;
     const float c0 = lane < k ? cj[lane] : 0.f;
     const float c1 = lane + 32 < k ? cj[lane + 32] : 0.f;
     float ex[RPW];
@@ -259,7 +263,8 @@ static int launch(const StoreView& sv, int TT, const void* x, const void* B, con
                                                               static_cast<const T*>(C), static_cast<const T*>(dt));
   if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
   auto kern = replay_verify_kernel<P, N, T, RC>;
-  const size_t smem = fold_staging_bytes<P, N>(sv.cap) + static_cast<size_t>(TT) * (P + N) * sizeof(T);
+  const size_t smem = fold_staging_bytes<P, N>(sv.cap) + static_cast<size_t>(TT) * (P + N) * sizeof(T) +
+                      static_cast<size_t>(TT) * (sv.cap + 1) * sizeof(float);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)

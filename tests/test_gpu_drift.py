@@ -92,3 +92,41 @@ class _At:
 
 def _at(drawn, i):
     return _At(np.ascontiguousarray(drawn.store[:, i]), drawn.f64[:, i])
+
+
+def test_shared_checkpoint_error_accumulates_with_slow_decay():
+    """With heads whose decay is slow (A scaled by 1e-3, so a window keeps ~99.8 % of the
+    state), a shared bf16 checkpoint's rounding error is fed back every window and adds up,
+    while a bf16 read copy's error stays a read error. Source: the post's section "Benefit 3"
+    (a shared low-precision checkpoint accumulates error with length; keeping the recurrence
+    in FP32 removes the growth). Reported per 256 tokens; checked: the read copy's error does
+    not grow, and at the end the shared checkpoint's error is the larger."""
+    steps, L, seed, chunk = 2048, 16, 43, 256
+    shape = sg.LayerShape(64, 8, 64, 128, 1, "f32")
+    sel = np.array([1, 33])
+    A, D = sg.head_params(shape.nheads, seed)
+    A = (A * np.float32(1e-3)).astype(np.float32)
+    stores = {}
+    for name, shared in (("bf16_read_copy", 0), ("shared_bf16_checkpoint", 1)):
+        cfg = R.ReplayConfig(64, 8, 64, 128, 1, L, 0, R.REPLAY_F32, R.REPLAY_RC_BF16, shared)
+        stores[name] = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
+    orc = Mamba2Decoder(A.astype(np.float64), D.astype(np.float64), 1, np.zeros((2, 8, 64, 128)))
+    y = {n: torch.empty(64, 8, 64, device="cuda") for n in stores}
+    mean = {n: np.zeros(steps) for n in stores}
+    for t0 in range(0, steps, 64):
+        d = sg.token_inputs(shape, seed, np.arange(t0, t0 + 64))
+        for i in range(64):
+            devs = [dev(_at(d[k], i), "f32") for k in ("x", "B", "C", "dt")]
+            for n, st in stores.items():
+                st.step(*devs, y[n])
+            yref = orc.step(*(d[k].f64[sel, i] for k in ("x", "B", "C", "dt")))
+            for n in stores:
+                mean[n][t0 + i] = rel_vec_err(y[n][sel].cpu().numpy(), yref, 2).mean()
+    report = {n: [float(mean[n][i:i + chunk].mean()) for i in range(0, steps, chunk)] for n in stores}
+    print(json.dumps({"slow_decay_mean_per_256": report}))
+    q = steps // 4
+    sep, shr = mean["bf16_read_copy"], mean["shared_bf16_checkpoint"]
+    assert sep[-q:].mean() <= 2.0 * sep[q:2 * q].mean() + 1e-9
+    assert shr[-q:].mean() > sep[-q:].mean()
+    for st in stores.values():
+        assert st.status() == 0
