@@ -641,17 +641,20 @@ def main(argv=None):
                     help="diagnostics: the read copy is the checkpoint (needs --read-copy)")
     ap.add_argument("--kernels-only", action="store_true",
                     help="diagnostics: time only the replay windows and print a short line (for ncu runs)")
+    ap.add_argument("--verify-only", action="store_true",
+                    help="diagnostics: run only the speculative verify workload and print its line")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line: batch x window sweep and 40-layer stack, "
                          "one JSON line per configuration")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
     rank, world, local_rank = dist_env()
-    if args.sweep:
+    if args.sweep or args.verify_only:
         import torch
         from hybrid_model_ssm_mamba_gb300 import replay as R
         torch.cuda.set_device(local_rank)
-        for line in run_sweep(torch, R):
+        lines = run_sweep(torch, R) if args.sweep else [run_speculative(torch, R, calls=args.steps)]
+        for line in lines:
             print(json.dumps(line), flush=True)
         return
     if args.impl == "reference":

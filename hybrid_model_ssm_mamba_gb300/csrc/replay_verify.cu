@@ -249,6 +249,203 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// FP32 checkpoint, dstate 128: the drafts' h0 . C_j on the tensor cores. h0 . [C_1 .. C_T] is
+// a 64 x 128 by 128 x T product per head; on CUDA cores with one warp reduction per draft it
+// made the kernel instruction-bound. Here each warp takes 8 rows of the slab and runs
+// mma.sync m16n8k8 with TF32 inputs and FP32 accumulation (rows 8..15 of the MMA tile are
+// zero padding). For FP32 accuracy both operands are split: h0 = hi + lo with hi the value
+// with its low 13 bits cleared (exact in TF32) and lo the exact remainder, and likewise C;
+// one MMA multiplies h0_hi and one h0_lo against B columns [C_hi of drafts 0..3 | C_lo of
+// drafts 0..3], which covers all four products; hi and lo columns are summed after. Lane
+// (g, q) = (lane / 4, lane % 4) holds row 8w + g, columns 16i + 4q .. 16i + 4q + 3 (i = 0..7),
+// loaded with one 16-byte load per i (each load of the warp reads 8 rows x 64 contiguous
+// bytes); the MMA k index q, q + 4 of k-tile 2i + h is column 16i + 4q + 2h, + 1. After the
+// MMAs, lane (g, q) finishes draft 2 (q & 1) + (q >> 1) of row 8w + g: the record terms from
+// records staged in shared memory, the decay, the skip term.
+__device__ __forceinline__ void mma_tf32_1688(float (&d)[4], unsigned a0, unsigned a2, unsigned b0, unsigned b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ unsigned tf32_hi(float v) { return __float_as_uint(v) & 0xFFFFE000u; }
+__device__ __forceinline__ unsigned tf32_lo(float v) { return __float_as_uint(v - __uint_as_float(tf32_hi(v))); }
+
+// Dynamic shared memory of the tensor-core verify kernel (bytes), in order: the fold staging
+// of a pre-fold; the drafts' C and x; the drafts' coefficients; the B fragments (per group of
+// 4 drafts: 16 k-tiles x 32 lanes x 2 words); each warp's 8 rows of the kk records' x.
+template <int P, int N, class T>
+constexpr size_t tc_verify_smem(int TT, int cap) {
+  return fold_staging_bytes<P, N>(cap) + static_cast<size_t>(TT) * (P + N) * sizeof(T) +
+         align128(static_cast<size_t>(TT) * (cap + 1) * sizeof(float)) +
+         static_cast<size_t>((TT + 3) / 4) * 16 * 32 * 2 * sizeof(unsigned) +
+         static_cast<size_t>(kWarps) * cap * 8 * sizeof(T);
+}
+
+template <int P, int N, class T>
+__global__ void __launch_bounds__(kThreads, 4)
+replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __restrict__ B,
+                        const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
+  static_assert(P == 64 && N == 128, "rows 8 per warp, 8 x 16 columns per row");
+  constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
+  constexpr int RCH = 8 * sizeof(T) / 16;  // 16-byte chunks of one record's 8 rows
+  extern __shared__ float4 smem4[];
+  __shared__ float s_red[kWarps];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, q = lane & 3;
+  const int H = sv.H, G = sv.G, cap = sv.cap;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int h = g * sv.hpg + blockIdx.x;
+  const int slab = b * H + h;
+  const int row = warp * 8 + gq;
+  auto xoff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * H * P + static_cast<size_t>(h) * P; };
+  auto boff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * G * N + static_cast<size_t>(g) * N; };
+
+  // shared memory regions
+  char* base = reinterpret_cast<char*>(smem4);
+  T* sq = reinterpret_cast<T*>(base + fold_staging_bytes<P, N>(cap));  // [TT][N] drafts' C
+  T* sx = sq + static_cast<size_t>(TT) * N;                                // [TT][P] drafts' x
+  float* s_cf = reinterpret_cast<float*>(sx + static_cast<size_t>(TT) * P);
+  unsigned* s_bf = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(s_cf) +
+                                               align128(static_cast<size_t>(TT) * (cap + 1) * sizeof(float)));
+  const int NG = (TT + 3) / 4;
+  T* s_xr = reinterpret_cast<T*>(s_bf + NG * 16 * 32 * 2) + static_cast<size_t>(warp) * cap * 8;
+
+  // Independent of the prep kernel: the lane's 32 checkpoint values, the drafts' C and x.
+  float a[8][4];
+  {
+    const float* hr = sv.h0 + static_cast<size_t>(slab) * P * N + static_cast<size_t>(row) * N + 4 * q;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ldv_stream<4>(hr + 16 * i, a[i]);
+  }
+  for (int c = tid; c < TT * (BC + XC); c += kThreads) {
+    if (c < TT * BC) {
+      const int j = c / BC, off = (c - j * BC) * EPC;
+      cp_async16(sq + j * N + off, C + boff(j) + off);
+    } else {
+      const int c2 = c - TT * BC;
+      const int j = c2 / XC, off = (c2 - j * XC) * EPC;
+      cp_async16(sx + j * P + off, x + xoff(j) + off);
+    }
+  }
+  cp_async_commit();
+  const float Dh = sv.D[h];
+
+  griddep_wait();  // plan and coefficients of this call are written
+  const int4 pl = sv.plan[b];
+  if (pl.z == kVerifyBad) {
+    cp_async_wait_all();
+    for (int j = 0; j < TT; ++j)
+      if (tid < P) y[xoff(j) + tid] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const int start = pl.x, n = pl.y;
+  const bool prefold = pl.z == kVerifyPrefold;
+  const int start2 = prefold ? ring_slot(start, n, cap) : start;
+  const int n2 = prefold ? 0 : n;
+  const int cs = cap + 1;
+  const float* cf = sv.coef + static_cast<size_t>(slab) * (sv.tmax + 1) * cs;
+  const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+  const int kk = n2 + TT;
+  // this warp's 8 rows of every record the drafts see (committed, then the drafts)
+  for (int c = lane; c < kk * RCH; c += 32) {
+    const int s = c / RCH, off = (c - s * RCH) * EPC;
+    const T* src = s < n2 ? ring.x + static_cast<size_t>(ring_slot(start2, s, cap)) * P : x + xoff(s - n2);
+    cp_async16(s_xr + s * 8 + off, src + warp * 8 + off);
+  }
+  cp_async_commit();
+
+  if (prefold) {  // a flush of the committed records, in the one-tile layout, then reload
+    using TL = Tile<P, N>;
+    float hv[TL::RPW][TL::E];
+    load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    float* sm_u = reinterpret_cast<float*>(smem4);
+    float* sm_b = sm_u + cap * P;
+    auto xf = [&](int s) { return ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P; };
+    auto bfn = [&](int s) { return ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N; };
+    stage_weighted<P, N, T>(xf, bfn, cf, n, sm_u, sm_b);
+    __syncthreads();
+    fold_staged<P, N>(sm_u, sm_b, n, cf[cap], hv);
+    write_checkpoint<P, N, REPLAY_RC_NONE>(sv, slab, s_red, hv, pl.w);
+    __syncthreads();  // the new checkpoint is written (and visible to the block)
+    const float* hr = sv.h0 + static_cast<size_t>(slab) * P * N + static_cast<size_t>(row) * N + 4 * q;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // L2 reads: the block's own writes of the new checkpoint
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(hr + 16 * i));
+      a[i][0] = v.x; a[i][1] = v.y; a[i][2] = v.z; a[i][3] = v.w;
+    }
+  }
+
+  // coefficients and B fragments (the drafts' C, split) into shared memory
+  for (int i = tid; i < TT * cs; i += kThreads) s_cf[i] = cf[cs + i];
+  cp_async_wait_group<1>();  // the drafts' C and x
+  __syncthreads();
+  for (int e = tid; e < NG * 16 * 32 * 2; e += kThreads) {
+    const int r = e & 1, L = (e >> 1) & 31, kt = (e >> 6) & 15, set = e >> 10;
+    const int gg = L >> 2, t = L & 3;
+    const int j = 4 * set + (gg & 3);
+    const int col = 16 * (kt >> 1) + 4 * t + 2 * (kt & 1) + r;
+    const float c = j < TT ? to_f(sq[j * N + col]) : 0.f;
+    s_bf[e] = (gg >> 2) ? tf32_lo(c) : tf32_hi(c);
+  }
+  cp_async_wait_all();  // this warp's records
+  __syncthreads();
+
+  // d[set]: the MMA accumulators of drafts 4 set .. 4 set + 3
+  float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  const uint2* bfr = reinterpret_cast<const uint2*>(s_bf) + lane;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float v0 = a[i][2 * hh], v1 = a[i][2 * hh + 1];
+      const unsigned h0 = tf32_hi(v0), h1 = tf32_hi(v1), l0 = tf32_lo(v0), l1 = tf32_lo(v1);
+#pragma unroll
+      for (int set = 0; set < 2; ++set) {
+        if (set < NG) {
+          const uint2 bb = bfr[(set * 16 + 2 * i + hh) * 32];
+          mma_tf32_1688(d[set], h0, h1, bb.x, bb.y);
+          mma_tf32_1688(d[set], l0, l1, bb.x, bb.y);
+        }
+      }
+    }
+  const int dsel = 2 * (q & 1) + (q >> 1);  // the draft (within a group of 4) this lane finishes
+#pragma unroll
+  for (int set = 0; set < 2; ++set) {
+    if (set >= NG) break;
+    // column 2q, 2q + 1 of row gq: q < 2 holds C_hi products of drafts 2q, 2q+1, q >= 2 the
+    // C_lo products of drafts 2(q-2), 2(q-2)+1
+    const float d0 = d[set][0] + __shfl_xor_sync(kFull, d[set][0], 2);
+    const float d1 = d[set][1] + __shfl_xor_sync(kFull, d[set][1], 2);
+    const int j = 4 * set + dsel;
+    if (j < TT) {
+      const float hc = (q >> 1) ? d1 : d0;
+      const int k = n2 + j + 1;  // records draft j sees, itself included
+      const float* cj = s_cf + j * cs;
+      float ex = 0.f;
+      for (int s = 0; s < k; ++s) ex = fmaf(cj[s], to_f(s_xr[s * 8 + gq]), ex);
+      y[xoff(j) + row] = fmaf(Dh, to_f(sx[j * P + row]), fmaf(cj[cap], hc, ex));
+    }
+  }
+  // the drafts' records go to the ring beyond the committed ones; the pointer stays
+  for (int j = 0; j < TT; ++j) {
+    const int slot = ring_slot(start2, n2 + j, cap);
+    if (tid < XC) {
+      *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
+          *reinterpret_cast<const uint4*>(x + xoff(j) + tid * EPC);
+    } else if (blockIdx.x == 0 && tid < XC + BC) {
+      const int c = tid - XC;
+      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+          *reinterpret_cast<const uint4*>(B + boff(j) + c * EPC);
+    } else if (tid == XC + BC) {
+      ring.dt[slot] = dt[(static_cast<size_t>(b) * TT + j) * H + h];
+    }
+  }
+}
+
 template <int P, int N, class T, int RC>
 static int launch(const StoreView& sv, int TT, const void* x, const void* B, const void* C,
                   const void* dt, float* y, cudaStream_t stream) {
@@ -263,8 +460,12 @@ static int launch(const StoreView& sv, int TT, const void* x, const void* B, con
                                                               static_cast<const T*>(C), static_cast<const T*>(dt));
   if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
   auto kern = replay_verify_kernel<P, N, T, RC>;
-  const size_t smem = fold_staging_bytes<P, N>(sv.cap) + static_cast<size_t>(TT) * (P + N) * sizeof(T) +
-                      static_cast<size_t>(TT) * (sv.cap + 1) * sizeof(float);
+  size_t smem = fold_staging_bytes<P, N>(sv.cap) + static_cast<size_t>(TT) * (P + N) * sizeof(T) +
+                static_cast<size_t>(TT) * (sv.cap + 1) * sizeof(float);
+  if constexpr (RC == REPLAY_RC_NONE && N == 128) {
+    kern = replay_verify_tc_kernel<P, N, T>;
+    smem = tc_verify_smem<P, N, T>(TT, sv.cap);
+  }
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)

@@ -269,6 +269,33 @@ def test_verify_workload_shape(rc):
     assert st.status() == 0
 
 
+@pytest.mark.parametrize("T", [1, 5, 8])
+def test_verify_draft_counts_bf16(T):
+    """Draft counts below, across and at the top of the tensor-core kernel's groups of four
+    drafts, bf16 inputs, 4 groups; commits leave up to L - 1 + T records so that verifies
+    also pre-fold. Every output and the final state against the oracle."""
+    shape = sg.LayerShape(6, 16, 64, 128, 4, "bf16")
+    L = 8
+    st, A, D = make_store(shape, 13, L=L, T=T)
+    orc = Mamba2Decoder(A, D, 4, np.zeros((6, 16, 64, 128)))
+    y = torch.empty(6, T, 16, 64, device="cuda")
+    worst = 0.0
+    for call in range(12):
+        devs, f64 = draft_device(shape, 13, call, T)
+        st.verify(T, *devs, y)
+        worst = max(worst, rel_vec_err(y.cpu().numpy(), orc.verify(*f64), 3).max())
+        acc = sg.accept_lengths(6, T, 13, call)
+        if call % 4 == 1:
+            acc[:] = T
+        st.commit(torch.from_numpy(acc).cuda())
+        orc.commit(acc, f64[0], f64[1], f64[3])
+    assert worst <= TOL, worst
+    h = torch.empty(6, 16, 64, 128, device="cuda")
+    st.export_state(h)
+    assert rel_vec_err(h.cpu().numpy(), orc.h, 2).max() <= TOL
+    assert st.status() == 0
+
+
 def test_bad_accept_sets_status_and_commits_nothing():
     shape = sg.LayerShape(2, 2, 64, 128, 1, "f32")
     st, _, _ = make_store(shape, 13, L=4, T=2)
