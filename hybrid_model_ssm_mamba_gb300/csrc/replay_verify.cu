@@ -281,16 +281,15 @@ constexpr size_t tc_verify_smem(int TT, int cap) {
   return fold_staging_bytes<P, N>(cap) + static_cast<size_t>(TT) * (P + N) * sizeof(T) +
          align128(static_cast<size_t>(TT) * (cap + 1) * sizeof(float)) +
          static_cast<size_t>((TT + 3) / 4) * 16 * 32 * 2 * sizeof(unsigned) +
-         static_cast<size_t>(kWarps) * cap * 8 * sizeof(T);
+         static_cast<size_t>(cap) * P * sizeof(T);
 }
 
 template <int P, int N, class T>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 3)
 replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __restrict__ B,
                         const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
   static_assert(P == 64 && N == 128, "rows 8 per warp, 8 x 16 columns per row");
   constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
-  constexpr int RCH = 8 * sizeof(T) / 16;  // 16-byte chunks of one record's 8 rows
   extern __shared__ float4 smem4[];
   __shared__ float s_red[kWarps];
 
@@ -301,8 +300,10 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   const int h = g * sv.hpg + blockIdx.x;
   const int slab = b * H + h;
   const int row = warp * 8 + gq;
-  auto xoff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * H * P + static_cast<size_t>(h) * P; };
-  auto boff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * G * N + static_cast<size_t>(g) * N; };
+  const T* xb = x + static_cast<size_t>(b) * TT * H * P + static_cast<size_t>(h) * P;  // draft j: + j H P
+  const T* cb = C + static_cast<size_t>(b) * TT * G * N + static_cast<size_t>(g) * N;  // draft j: + j G N
+  const T* bb = B + static_cast<size_t>(b) * TT * G * N + static_cast<size_t>(g) * N;
+  float* yb = y + static_cast<size_t>(b) * TT * H * P + static_cast<size_t>(h) * P;
 
   // shared memory regions
   char* base = reinterpret_cast<char*>(smem4);
@@ -312,9 +313,11 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   unsigned* s_bf = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(s_cf) +
                                                align128(static_cast<size_t>(TT) * (cap + 1) * sizeof(float)));
   const int NG = (TT + 3) / 4;
-  T* s_xr = reinterpret_cast<T*>(s_bf + NG * 16 * 32 * 2) + static_cast<size_t>(warp) * cap * 8;
+  T* s_rec = reinterpret_cast<T*>(s_bf + NG * 16 * 32 * 2);  // [n2][P] committed records' x
 
-  // Independent of the prep kernel: the lane's 32 checkpoint values, the drafts' C and x.
+  // Independent of the prep kernel: the lane's 32 checkpoint values, the drafts' C and x in
+  // shared memory, and each thread's share of the drafts' records to append (x of this
+  // head, B of the group by the group's first head, dt) in registers.
   float a[8][4];
   {
     const float* hr = sv.h0 + static_cast<size_t>(slab) * P * N + static_cast<size_t>(row) * N + 4 * q;
@@ -324,14 +327,30 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   for (int c = tid; c < TT * (BC + XC); c += kThreads) {
     if (c < TT * BC) {
       const int j = c / BC, off = (c - j * BC) * EPC;
-      cp_async16(sq + j * N + off, C + boff(j) + off);
+      cp_async16(sq + j * N + off, cb + static_cast<size_t>(j) * G * N + off);
     } else {
       const int c2 = c - TT * BC;
       const int j = c2 / XC, off = (c2 - j * XC) * EPC;
-      cp_async16(sx + j * P + off, x + xoff(j) + off);
+      cp_async16(sx + j * P + off, xb + static_cast<size_t>(j) * H * P + off);
     }
   }
   cp_async_commit();
+  const int nxc = TT * XC, nbc = blockIdx.x == 0 ? TT * BC : 0, napp = nxc + nbc + TT;
+  uint4 app[2];
+  T appdt[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int c = tid + r * kThreads;
+    if (c < nxc) {
+      const int j = c / XC, off = (c - j * XC) * EPC;
+      app[r] = *reinterpret_cast<const uint4*>(xb + static_cast<size_t>(j) * H * P + off);
+    } else if (c < nxc + nbc) {
+      const int c2 = c - nxc, j = c2 / BC, off = (c2 - j * BC) * EPC;
+      app[r] = *reinterpret_cast<const uint4*>(bb + static_cast<size_t>(j) * G * N + off);
+    } else if (c < napp) {
+      appdt[r] = dt[(static_cast<size_t>(b) * TT + (c - nxc - nbc)) * H + h];
+    }
+  }
   const float Dh = sv.D[h];
 
   griddep_wait();  // plan and coefficients of this call are written
@@ -339,7 +358,7 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   if (pl.z == kVerifyBad) {
     cp_async_wait_all();
     for (int j = 0; j < TT; ++j)
-      if (tid < P) y[xoff(j) + tid] = __int_as_float(0x7fc00000);
+      if (tid < P) yb[static_cast<size_t>(j) * H * P + tid] = __int_as_float(0x7fc00000);
     return;
   }
   const int start = pl.x, n = pl.y;
@@ -349,14 +368,27 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   const int cs = cap + 1;
   const float* cf = sv.coef + static_cast<size_t>(slab) * (sv.tmax + 1) * cs;
   const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
-  const int kk = n2 + TT;
-  // this warp's 8 rows of every record the drafts see (committed, then the drafts)
-  for (int c = lane; c < kk * RCH; c += 32) {
-    const int s = c / RCH, off = (c - s * RCH) * EPC;
-    const T* src = s < n2 ? ring.x + static_cast<size_t>(ring_slot(start2, s, cap)) * P : x + xoff(s - n2);
-    cp_async16(s_xr + s * 8 + off, src + warp * 8 + off);
+  // the committed records the drafts see (a pre-fold folds them first: then there are none)
+  for (int c = tid; c < n2 * XC; c += kThreads) {
+    const int s = c / XC, off = (c - s * XC) * EPC;
+    cp_async16(s_rec + s * P + off, ring.x + static_cast<size_t>(ring_slot(start2, s, cap)) * P + off);
   }
   cp_async_commit();
+  // the drafts' records go to the ring beyond the committed ones; the pointer stays
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int c = tid + r * kThreads;
+    if (c < nxc) {
+      const int j = c / XC, off = (c - j * XC) * EPC;
+      *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(ring_slot(start2, n2 + j, cap)) * P + off) = app[r];
+    } else if (c < nxc + nbc) {
+      const int c2 = c - nxc, j = c2 / BC, off = (c2 - j * BC) * EPC;
+      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(ring_slot(start2, n2 + j, cap)) * N + off) = app[r];
+    } else if (c < napp) {
+      const int j = c - nxc - nbc;
+      ring.dt[ring_slot(start2, n2 + j, cap)] = appdt[r];
+    }
+  }
 
   if (prefold) {  // a flush of the committed records, in the one-tile layout, then reload
     using TL = Tile<P, N>;
@@ -391,7 +423,7 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
     const float c = j < TT ? to_f(sq[j * N + col]) : 0.f;
     s_bf[e] = (gg >> 2) ? tf32_lo(c) : tf32_hi(c);
   }
-  cp_async_wait_all();  // this warp's records
+  cp_async_wait_all();  // the committed records
   __syncthreads();
 
   // d[set]: the MMA accumulators of drafts 4 set .. 4 set + 3
@@ -423,25 +455,11 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
     const int j = 4 * set + dsel;
     if (j < TT) {
       const float hc = (q >> 1) ? d1 : d0;
-      const int k = n2 + j + 1;  // records draft j sees, itself included
       const float* cj = s_cf + j * cs;
-      float ex = 0.f;
-      for (int s = 0; s < k; ++s) ex = fmaf(cj[s], to_f(s_xr[s * 8 + gq]), ex);
-      y[xoff(j) + row] = fmaf(Dh, to_f(sx[j * P + row]), fmaf(cj[cap], hc, ex));
-    }
-  }
-  // the drafts' records go to the ring beyond the committed ones; the pointer stays
-  for (int j = 0; j < TT; ++j) {
-    const int slot = ring_slot(start2, n2 + j, cap);
-    if (tid < XC) {
-      *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
-          *reinterpret_cast<const uint4*>(x + xoff(j) + tid * EPC);
-    } else if (blockIdx.x == 0 && tid < XC + BC) {
-      const int c = tid - XC;
-      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
-          *reinterpret_cast<const uint4*>(B + boff(j) + c * EPC);
-    } else if (tid == XC + BC) {
-      ring.dt[slot] = dt[(static_cast<size_t>(b) * TT + j) * H + h];
+      float ex = 0.f;  // records draft j sees: the n2 committed ones, then drafts 0..j
+      for (int s = 0; s < n2; ++s) ex = fmaf(cj[s], to_f(s_rec[s * P + row]), ex);
+      for (int s = 0; s <= j; ++s) ex = fmaf(cj[n2 + s], to_f(sx[s * P + row]), ex);
+      yb[static_cast<size_t>(j) * H * P + row] = fmaf(Dh, to_f(sx[j * P + row]), fmaf(cj[cap], hc, ex));
     }
   }
 }

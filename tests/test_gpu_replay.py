@@ -11,7 +11,7 @@ import synthgen as sg
 from gpu_util import DTYPE, draft_device, make_store, rel_vec_err, step_inputs
 from hybrid_model_ssm_mamba_gb300 import replay as R
 from oracle import formats as F
-from oracle.mamba2 import Mamba2Decoder
+from oracle.mamba2 import Mamba2Decoder, window_output
 from test_gpu_nvfp4 import device_codes
 
 pytestmark = pytest.mark.gpu
@@ -358,7 +358,8 @@ def test_fused_and_split_step_paths_agree():
     assert rel_vec_err(outs[1], outs[0], 3).max() <= 1e-5
 
 
-@pytest.mark.parametrize("rc,bound", [(R.REPLAY_RC_BF16, 1e-2), (R.REPLAY_RC_FP8E4M3, 0.25)])
+@pytest.mark.parametrize("rc,bound", [(R.REPLAY_RC_BF16, 1e-2), (R.REPLAY_RC_FP8E4M3, 0.25),
+                                      (R.REPLAY_RC_FP16, 2e-3)])
 def test_read_copy_on_the_large_call_path(rc, bound):
     """Above the fused-kernel threshold a read copy is read by CTAs that each take several
     heads of a group (packed copy tiles). 72 sequences x 128 heads, 8 groups, across two
@@ -379,6 +380,48 @@ class _SrRounder:
         out = F.fp16_sr_round_state(h, self.epoch, self.sel, self.num_slabs)
         self.epoch += 1
         return out
+
+
+def _decoded_copy(st, rc, h32):
+    """The values a non-flush step reads from the copy of FP32 states h32 [b, H, P, N]."""
+    if rc == R.REPLAY_RC_BF16:
+        return F.bf16_decode(F.bf16_encode(h32)).astype(np.float64)
+    if rc == R.REPLAY_RC_FP16:
+        return F.fp16_decode(F.fp16_encode(h32))
+    out = np.empty(h32.shape)
+    for i in np.ndindex(*h32.shape[:2]):
+        qc, sc = F.fp8_slab_quantize(h32[i])
+        out[i] = F.fp8_slab_dequantize(qc, sc)
+    return out
+
+
+@pytest.mark.parametrize("rc", [R.REPLAY_RC_BF16, R.REPLAY_RC_FP16, R.REPLAY_RC_FP8E4M3])
+@pytest.mark.parametrize("batch,heads,groups,dtype", [(4, 8, 2, "f32"), (72, 128, 8, "bf16")])
+def test_copy_reads_follow_the_decoded_copy(rc, batch, heads, groups, dtype):
+    """Non-flush outputs against the unrolled window evaluated in FP64 from the copy's own
+    values (the format's decoding of the loaded FP32 state), within 1e-4: the copy is read
+    exactly, whichever kernel reads it (the fused small-call kernel; on the large call the
+    tensor-core kernel for bf16 and FP16, the several-heads kernel for E4M3)."""
+    shape = sg.LayerShape(batch, heads, 64, 128, groups, dtype)
+    L, seed = 8, 31
+    st, A, D = make_store(shape, seed, L=L, read_copy=rc)
+    sel = np.array([0, batch - 1])
+    h0 = sg.initial_state(shape, seed)
+    st.load_state(torch.from_numpy(h0).cuda())
+    hread = _decoded_copy(st, rc, h0[sel])
+    y = torch.empty(batch, heads, 64, device="cuda")
+    rec = {k: [] for k in ("x", "B", "dt")}
+    worst = 0.0
+    for t in range(L - 1):
+        devs, f64 = step_inputs(shape, seed, t, sel)
+        st.step(*devs, y)
+        for k, v in zip(("x", "B", "dt"), (f64[0], f64[1], f64[3])):
+            rec[k].append(v)
+        ywin = window_output(hread, np.stack(rec["x"], 1), np.stack(rec["B"], 1), np.stack(rec["dt"], 1),
+                             f64[2], A, D)
+        worst = max(worst, rel_vec_err(y[sel].cpu().numpy(), ywin, 2).max())
+    assert worst <= TOL, worst
+    assert st.status() == 0
 
 
 @pytest.mark.parametrize("rc,tol", [(R.REPLAY_RC_BF16, 5e-3), (R.REPLAY_RC_FP8E4M3, 5e-2),
