@@ -235,6 +235,28 @@ __device__ __forceinline__ RecordWeights record_weights(float dt0, float dt1, in
   return r;
 }
 
+// The same for two heads at once when k <= 16: lanes 0..15 carry records 0..15 of one head,
+// lanes 16..31 those of the other, with each half-warp's own A. Suffix sums stay within a
+// half-warp; w is the weight of the lane's record, gam its head's cumulative decay.
+struct HalfWeights {
+  float w, gam;
+};
+__device__ __forceinline__ HalfWeights record_weights_pair(float dtv, int k, float A, int lane) {
+  const int hl = lane & 15;
+  float in = dtv;
+#pragma unroll
+  for (int off = 1; off < 16; off <<= 1) {
+    const float a = __shfl_down_sync(kFull, in, off, 16);
+    if (hl + off < 16) in += a;
+  }
+  float ex = __shfl_down_sync(kFull, in, 1, 16);  // exclusive: the records after s
+  if (hl == 15) ex = 0.f;
+  HalfWeights r;
+  r.w = hl < k ? __expf(A * ex) * dtv : 0.f;
+  r.gam = __expf(A * __shfl_sync(kFull, in, lane & 16));
+  return r;
+}
+
 // Fold K records into the register tile of the checkpoint, record s at image slot
 // slot_of(s) ("How ReplaySSM represents the state": the state after a window is the
 // cumulative decay times the state before it, plus the buffered records):

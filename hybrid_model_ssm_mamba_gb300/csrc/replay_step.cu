@@ -101,6 +101,23 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
     }
   }
   __syncthreads();
+  if (k <= 16) {  // two heads per warp: half-warp scans
+    for (int hp = 2 * warp; hp < sv.hpg; hp += 2 * kPrepWarps) {
+      const int hh = hp + (lane >> 4), s = lane & 15;
+      const bool live = hh < sv.hpg;
+      const int h = g * sv.hpg + (live ? hh : hp);
+      const size_t slab = static_cast<size_t>(b) * sv.H + h;
+      const T* dtr = static_cast<const T*>(sv.dtbuf) + slab * cap;
+      float dtv = 0.f;
+      if (live && s < k)
+        dtv = stage_dt ? s_dt[hh * k + s] : to_f(s < n ? dtr[ring_slot(start, s, cap)] : dt[slab]);
+      const HalfWeights rw = record_weights_pair(dtv, k, sv.A[h], lane);
+      float* cf = sv.coef + slab * (cap + 1);
+      if (live && s < k) cf[s] = flush ? rw.w : rw.w * s_bc[s];
+      if (live && s == 0) cf[cap] = rw.gam;
+    }
+    return;
+  }
   for (int hh = warp; hh < sv.hpg; hh += kPrepWarps) {
     const int h = g * sv.hpg + hh;
     const size_t slab = static_cast<size_t>(b) * sv.H + h;

@@ -128,6 +128,43 @@ def test_window_length_invariance(L):
     assert wy <= TOL and wh <= TOL, (L, wy, wh)
 
 
+@pytest.mark.parametrize("batch,heads,groups,dtype,read_copy", [
+    (2, 8, 2, "f32", R.REPLAY_RC_NONE), (72, 128, 8, "bf16", R.REPLAY_RC_NONE),
+    (72, 128, 8, "bf16", R.REPLAY_RC_BF16)])
+def test_longest_window(batch, heads, groups, dtype, read_copy):
+    """L = 64, the most records a ring holds without verify: non-flush steps with more than 32
+    buffered records (lanes s and s + 32 both carry records), one flush of 64 records."""
+    shape = sg.LayerShape(batch, heads, 64, 128, groups, dtype)
+    wy, wh, _, _ = run_decode(shape, 72, 64, seed=37, read_copy=read_copy, seqs=[0, batch - 1])
+    bound = TOL if read_copy == R.REPLAY_RC_NONE else 1e-2
+    assert wy <= bound and wh <= TOL, (wy, wh)
+
+
+def test_verify_fullest_ring():
+    """L = 49 and T = 8 give a ring of 64 records; commits of all drafts push the committed
+    count to L - 1 + T = 56 before a verify pre-folds, so record lanes past 32 are used."""
+    shape = sg.LayerShape(4, 8, 64, 128, 2, "f32")
+    T, L = 8, 49
+    st, A, D = make_store(shape, 39, L=L, T=T)
+    assert st.layout.cap == 64
+    orc = Mamba2Decoder(A, D, 2, np.zeros((4, 8, 64, 128)))
+    y = torch.empty(4, T, 8, 64, device="cuda")
+    worst = 0.0
+    for call in range(10):
+        devs, f64 = draft_device(shape, 39, call, T)
+        st.verify(T, *devs, y)
+        worst = max(worst, rel_vec_err(y.cpu().numpy(), orc.verify(*f64), 3).max())
+        acc = np.full(4, T, dtype=np.int32)
+        acc[1] = call % (T + 1)
+        st.commit(torch.from_numpy(acc).cuda())
+        orc.commit(acc, f64[0], f64[1], f64[3])
+    assert worst <= TOL, worst
+    h = torch.empty(4, 8, 64, 128, device="cuda")
+    st.export_state(h)
+    assert rel_vec_err(h.cpu().numpy(), orc.h, 2).max() <= TOL
+    assert st.status() == 0
+
+
 def test_replay_equals_conventional_gpu():
     """GPU replay == GPU load-update-store on the same inputs (bf16 inputs, FP32 state)."""
     shape = sg.LayerShape(4, 16, 64, 128, 4, "bf16")
