@@ -142,6 +142,13 @@ int replay_alloc(const replay_config* c, void* workspace, size_t workspace_bytes
   sv.cap = L.cap;
   sv.tmax = c->max_draft_T;
   sv.shared = c->shared_checkpoint;
+  int dev = 0;
+  sv.sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sv.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    sv.sms = 0;
+    (void)cudaGetLastError();
+  }
   st->sh = rssm::Shape{c->headdim, c->dstate, c->in_dtype, c->read_copy};
   rc = replay_reset(st, nullptr, stream);
   if (rc != REPLAY_OK) {

@@ -18,6 +18,9 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCap = 64;    // ring records a sequence can hold (2 per lane)
 constexpr int kDtStage = 1024; // dt values a prep CTA stages in shared memory at once
 constexpr unsigned kFull = 0xffffffffu;
+// Dynamic shared memory above this opts the kernel in to more than the default 48 KB per CTA,
+// a cap that counts static shared memory too (at most about 6 KB in these kernels).
+constexpr size_t kSmemNoOptIn = 40 * 1024;
 constexpr float kE4M3Max = 448.0f;
 
 // Resident CTAs per SM the register budget is sized for: a P=64 slab tile is 8 rows x N/32
@@ -45,7 +48,16 @@ struct StoreView {
   const float* D;
   int batch, H, G, hpg, L, cap, tmax;
   int shared;     // 1: the read copy is the checkpoint (no FP32 checkpoint)
+  int sms;        // SMs of the device the store lives on (0: unknown, no L2 prefetch)
 };
+
+// Bulk prefetch of `bytes` (a multiple of 16, from a 16-byte aligned address) into L2: one
+// instruction, no registers held, nothing to wait for. A per-head kernel CTA prefetches the
+// state a CTA one wave later will read, so DRAM keeps streaming while the resident CTAs
+// compute (their own loads are bounded by the registers that receive them).
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned int bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // ------------------------------------------------------------------ element conversion
 __device__ __forceinline__ float to_f(float v) { return v; }
@@ -278,6 +290,23 @@ __device__ __forceinline__ void load_tile_f32(const float* slab, int warp, int l
     for (int v = 0; v < TL::NVEC; ++v) {
       float t[TL::VEC];
       ldv_stream<TL::VEC>(slab + TL::row(warp, i) * N + TL::col(lane, v), t);
+#pragma unroll
+      for (int e = 0; e < TL::VEC; ++e) hv[i][v * TL::VEC + e] = t[e];
+    }
+}
+
+// The same tile from a row-major FP32 slab in shared memory (a warp's access covers one row:
+// conflict-free).
+template <int P, int N>
+__device__ __forceinline__ void load_tile_smem(const float* slab, int warp, int lane,
+                                               float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i)
+#pragma unroll
+    for (int v = 0; v < TL::NVEC; ++v) {
+      float t[TL::VEC];
+      ldv<TL::VEC>(slab + TL::row(warp, i) * N + TL::col(lane, v), t);
 #pragma unroll
       for (int e = 0; e < TL::VEC; ++e) hv[i][v * TL::VEC + e] = t[e];
     }
@@ -572,6 +601,59 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// One-shot bulk copy global -> shared by the tensor memory accelerator, tracked by an
+// mbarrier in shared memory: one thread initialises the barrier (count 1), arms it with the
+// byte count, issues the copy and later waits on phase 0 while the others wait at a CTA
+// barrier (spinning warps would take issue slots from the SM's other CTAs). The data never passes
+// through registers or L1, so a CTA keeps its whole slab in flight however few registers it
+// has. Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(unsigned long long* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(bar)) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// The copy is marked evict-first in L2 (read once per call), like the streaming loads, so
+// the state stream does not push the ring records out of L2.
+__device__ __forceinline__ void bulk_load(void* smem, const void* gmem, unsigned int bytes, unsigned long long* bar) {
+  unsigned long long policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(policy));
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n" ::"r"(
+          smem_u32(smem)),
+      "l"(gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+// Wait for phase `parity` of the barrier for at most about `ns` nanoseconds of the global
+// timer (and a fixed number of polls); false if it has not completed by then.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned int parity, unsigned long long ns) {
+  const unsigned a = smem_u32(bar);
+  unsigned long long t0 = 0;
+  for (int it = 0; it < (1 << 28); ++it) {
+    unsigned done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 255) == 0) {
+      const unsigned long long t = global_ns();
+      if (it == 0) t0 = t;
+      else if (t - t0 > ns) return false;
+    }
+  }
+  return false;
+}
+constexpr unsigned long long kCopyWaitNs = 1000000000ull;  // 1 s: far beyond any copy's time
 
 // Programmatic dependent launch: a primary kernel lets its dependent start early; the
 // dependent waits, where it first needs the primary's results, until the primary grid has

@@ -198,6 +198,28 @@ __device__ __forceinline__ float tile_rows_dot(const float (&hv)[Tile<P, N>::RPW
   return warp_transpose_reduce<TL::RPW>(part, lane);
 }
 
+// The same output with the tile read row by row from a row-major FP32 slab in shared
+// memory: a row's E values are live at a time, not the whole tile.
+template <int P, int N>
+__device__ __forceinline__ float smem_rows_dot(const float* slab, const float (&cv)[Tile<P, N>::E], float gam,
+                                               const float (&extra)[Tile<P, N>::RPW], int warp, int lane) {
+  using TL = Tile<P, N>;
+  float part[TL::RPW];
+#pragma unroll
+  for (int i = 0; i < TL::RPW; ++i) {
+    float hc = 0.f;
+#pragma unroll
+    for (int v = 0; v < TL::NVEC; ++v) {
+      float t[TL::VEC];
+      ldv<TL::VEC>(slab + TL::row(warp, i) * N + TL::col(lane, v), t);
+#pragma unroll
+      for (int e = 0; e < TL::VEC; ++e) hc = fmaf(t[e], cv[v * TL::VEC + e], hc);
+    }
+    part[i] = fmaf(gam, hc, extra[i]);
+  }
+  return warp_transpose_reduce<TL::RPW>(part, lane);
+}
+
 // Weights of the records of one query, one record per lane (record s = lane, and lane+32
 // when k > 32): w_s = exp(A sum_{r=s+1..k-1} dt_r) * dt_s, Gamma = exp(A sum_{r<k} dt_r).
 // The suffix sums are warp scans (tree order) over the records' dt, each over its own range.

@@ -98,7 +98,7 @@ template <int P, int N, class T, int RC>
 static int fold(const StoreView& sv, int mode, float* out, cudaStream_t stream) {
   const size_t smem = smem_plan_bytes<P, N>(ring_image_bytes<P, N, T>(sv.cap), sv.cap);
   auto kern = mode == 0 ? replay_fold_kernel<P, N, T, RC, 0> : replay_fold_kernel<P, N, T, RC, 1>;
-  if (smem > 48 * 1024 &&
+  if (smem > kSmemNoOptIn &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;

@@ -135,8 +135,36 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
   }
 }
 
+// The state bytes of slabs [slab, slab + nslab) as a per-head kernel reads them: the FP32
+// checkpoint, or the read copy (NVFP4: codes and block scales).
+template <int P, int N, int RC>
+__device__ __forceinline__ void prefetch_slabs(const StoreView& sv, long long slab, int nslab, bool f32) {
+  if (f32) {
+    prefetch_l2(sv.h0 + slab * P * N, nslab * (P * N * 4u));
+  } else if constexpr (RC == REPLAY_RC_NVFP4) {
+    prefetch_l2(static_cast<const uint8_t*>(sv.rc) + slab * (P * N / 2), nslab * (P * N / 2u));
+    prefetch_l2(sv.bscale + slab * (P * N / kFp4Block), nslab * (P * N / static_cast<unsigned>(kFp4Block)));
+  } else if constexpr (RC != REPLAY_RC_NONE) {
+    constexpr unsigned esz = RC == REPLAY_RC_FP8E4M3 ? 1u : 2u;
+    prefetch_l2(static_cast<const uint8_t*>(sv.rc) + slab * P * N * esz, nslab * (P * N * esz));
+  }
+}
+
+// A CTA covering slabs [slab0, slab0 + nslab) sends to L2 the slabs of the CTA one wave
+// (SMs x resident CTAs per SM) after it: CTAs of these grids run in slab order, so that CTA
+// starts about when this one ends, and finds its state in L2.
+template <int P, int N, int RC>
+__device__ __forceinline__ void prefetch_next_wave(const StoreView& sv, int slab0, int nslab, int ctas_per_sm,
+                                                   bool f32) {
+  if (threadIdx.x != 0 || sv.sms <= 0) return;
+  const long long ahead = slab0 + static_cast<long long>(sv.sms) * ctas_per_sm * nslab;
+  if (ahead + nslab <= static_cast<long long>(sv.batch) * sv.H) prefetch_slabs<P, N, RC>(sv, ahead, nslab, f32);
+}
+
 // expect_flush: the host knows every sequence flushes on this step, so a CTA with a read copy
-// loads the FP32 checkpoint (the flush's input) before the prep wait instead of the copy.
+// loads the FP32 checkpoint (the flush's input) before the prep wait instead of the copy, and
+// every CTA sends the slab of the CTA one wave later to L2 (a flush computes between its read
+// and its write, so its own loads leave DRAM idle part of the time).
 template <int P, int N, class T, int RC>
 __global__ void __launch_bounds__(kThreads, kMinBlocks<N>)
 replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
@@ -159,6 +187,7 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
   // Independent of the prep kernel: the slab the step most likely reads, C, x for D x.
   float hv[RPW][E];
   const bool f32_first = RC == REPLAY_RC_NONE || (expect_flush && !sv.shared);
+  if (expect_flush) prefetch_next_wave<P, N, RC>(sv, slab, 1, kMinBlocks<N>, f32_first);
   auto load_copy = [&] {
     if constexpr (RC != REPLAY_RC_NONE) {
       const float scale = RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4 ? sv.scale[slab] : 1.f;
@@ -223,6 +252,140 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
   const float sum = tile_rows_dot<P, N>(hv, cv, 1.f, zero, lane);
   if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
   write_checkpoint<P, N, RC>(sv, slab, s_red, hv, pl.w);
+}
+
+// ---------------------------------------------------------------------------------------
+// replay_step_read_kernel: the FP32-checkpoint step when the host knows that no sequence
+// flushes (the non-flush steps of a window). Such a step only reads, so its speed is the
+// bytes an SM keeps in flight. A register tile holds 32 KB per CTA and the register file
+// allows 4 such CTAs; loads into registers also pass through L1, which a shared-memory
+// carveout shrinks. Here one thread brings the slab into shared memory with one bulk copy
+// (neither registers nor L1 hold it in flight), the dot products stream from shared memory
+// row by row, and the few registers left let kReadCtas CTAs share an SM. A flush plan, not
+// expected here, folds a quarter of a warp's rows at a time with the records read from
+// global memory.
+template <int N>
+constexpr int kReadCtas = N >= 256 ? 3 : 6;
+
+template <int P, int N, class T>
+__global__ void __launch_bounds__(kThreads, kReadCtas<N>)
+replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
+                        const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
+  using TL = Tile<P, N>;
+  constexpr int RPW = TL::RPW, E = TL::E, VEC = TL::VEC, NVEC = TL::NVEC, HR = RPW / 4;
+  constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
+  extern __shared__ float4 smem4[];
+  __shared__ __align__(8) unsigned long long s_bar;
+  __shared__ int s_landed;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int h = g * sv.hpg + blockIdx.x;
+  const int slab = b * sv.H + h;
+  const int cap = sv.cap;
+  const size_t xo = static_cast<size_t>(slab) * P;
+  const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
+  float* s_h = reinterpret_cast<float*>(smem4);
+  float* h0 = sv.h0 + static_cast<size_t>(slab) * P * N;
+  if (tid == 0) {
+    mbar_init(&s_bar);
+    bulk_load(s_h, h0, P * N * sizeof(float), &s_bar);
+  }
+  float cv[E];
+  load_cols<P, N>(C + bo, lane, cv);
+  const int myrow = warp * RPW + transpose_index<RPW>(lane);
+  const float xk_row = to_f(x[xo + myrow]);
+  const float Dh = sv.D[h];
+
+  griddep_wait();  // plan and coefficients of this step are written
+  const int4 pl = sv.plan[b];
+  const int start = pl.x, n = pl.y, k = n + 1;
+  const float* cf = sv.coef + static_cast<size_t>(slab) * (cap + 1);
+  const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+  auto x_of = [&](int s) { return s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P : x + xo; };
+  float xr[RPW];
+  if (pl.z == kPlanNonFlush) record_terms<RPW, T>(x_of, cf, k, warp, lane, xr);
+  // The slab must have landed before it is read or the CTA exits; one thread waits, the rest
+  // at the barrier. A copy past its limit leaves this slab's y NaN and its state untouched
+  // (after a second bounded wait).
+  if (tid == 0) {
+    const bool ok = mbar_wait(&s_bar, 0, kCopyWaitNs);
+    if (!ok) {
+      set_status(sv.status, REPLAY_DEV_COPY_TIMEOUT);
+      mbar_wait(&s_bar, 0, kCopyWaitNs);
+    }
+    s_landed = ok;
+  }
+  __syncthreads();
+  if (!s_landed || pl.z == kPlanBad) {
+    if (tid < P) y[xo + tid] = __int_as_float(0x7fc00000);
+    return;
+  }
+
+  if (pl.z == kPlanNonFlush) {
+    const float sum = smem_rows_dot<P, N>(s_h, cv, cf[cap], xr, warp, lane);
+    if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
+    const int slot = ring_slot(start, n, cap);
+    if (tid < XC) {
+      *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
+          *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
+    } else if (blockIdx.x == 0 && tid < XC + BC) {
+      const int c = tid - XC;
+      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+          *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+    } else if (tid == XC + BC) {
+      ring.dt[slot] = dt[slab];
+    }
+    return;
+  }
+
+  // flush: h <- Gamma h + sum_s w_s x_s B_s^T, a quarter of the warp's rows at a time
+  auto b_of = [&](int s) { return s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo; };
+  const float gam = cf[cap];
+  float part[RPW];
+#pragma unroll
+  for (int hf = 0; hf < 4; ++hf) {
+    const int r0 = warp * RPW + hf * HR;
+    float hv[HR][E];
+#pragma unroll
+    for (int i = 0; i < HR; ++i)
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v) {
+        float t[VEC];
+        ldv<VEC>(s_h + (r0 + i) * N + TL::col(lane, v), t);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) hv[i][v * VEC + e] = gam * t[e];
+      }
+    for (int s = 0; s < k; ++s) {
+      float bv[E];
+      load_cols<P, N>(b_of(s), lane, bv);
+      const T* xs = x_of(s) + r0;
+      const float w = cf[s];
+#pragma unroll
+      for (int i = 0; i < HR; ++i) {
+        const float ui = w * to_f(xs[i]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) hv[i][e] = fmaf(ui, bv[e], hv[i][e]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < HR; ++i) {
+      float hc = 0.f;
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v) {
+        float t[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          t[e] = hv[i][v * VEC + e];
+          hc = fmaf(t[e], cv[v * VEC + e], hc);
+        }
+        stv_stream<VEC>(h0 + (r0 + i) * N + TL::col(lane, v), t);
+      }
+      part[hf * HR + i] = hc;
+    }
+  }
+  const float sum = warp_transpose_reduce<RPW>(part, lane);
+  if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -750,7 +913,7 @@ constexpr long long kFusedMaxSlabs = 1024;
 // Launch a per-head kernel as a programmatic dependent of the prep kernel before it.
 template <class... KArgs, class... Args>
 static int pdl_launch(void (*kern)(KArgs...), dim3 grid, size_t smem, cudaStream_t stream, Args... args) {
-  if (smem > 48 * 1024 &&
+  if (smem > kSmemNoOptIn &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
@@ -781,7 +944,7 @@ static int launch(const StoreView& sv, int all_n, const void* x, const void* B, 
   if (static_cast<long long>(sv.batch) * sv.H <= kFusedMaxSlabs) {
     auto fused = replay_step_fused_kernel<P, N, T, RC>;
     const size_t fsmem = smem_plan_bytes<P, N>(whole_image_bytes<P, N, T>(sv.cap), sv.cap);
-    if (fsmem > 48 * 1024 &&
+    if (fsmem > kSmemNoOptIn &&
         cudaFuncSetAttribute(fused, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(fsmem)) !=
             cudaSuccess)
       return REPLAY_ECUDA;
@@ -790,7 +953,7 @@ static int launch(const StoreView& sv, int all_n, const void* x, const void* B, 
   }
   auto prep = replay_step_prep_kernel<P, N, T>;
   const size_t psmem = static_cast<size_t>(sv.cap + 1) * N * sizeof(T);
-  if (psmem > 48 * 1024 &&
+  if (psmem > kSmemNoOptIn &&
       cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
@@ -809,6 +972,11 @@ static int launch(const StoreView& sv, int all_n, const void* x, const void* B, 
     if (!all_flush && HPC > 1 && sv.hpg % HPC == 0)
       return pdl_launch(replay_step_copy_kernel<P, N, T, RC, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch), smem,
                         stream, sv, tx, tB, tC, tdt, y);
+  }
+  if constexpr (RC == REPLAY_RC_NONE) {
+    if (all_n >= 0 && !all_flush)
+      return pdl_launch(replay_step_read_kernel<P, N, T>, dim3(sv.hpg, sv.G, sv.batch),
+                        static_cast<size_t>(P) * N * sizeof(float), stream, sv, tx, tB, tC, tdt, y);
   }
   return pdl_launch(replay_step_kernel<P, N, T, RC>, dim3(sv.hpg, sv.G, sv.batch), smem, stream, sv, tx, tB, tC,
                     tdt, y, all_flush ? 1 : 0);

@@ -470,7 +470,7 @@ static int launch(const StoreView& sv, int TT, const void* x, const void* B, con
   const bool wide = static_cast<long long>(sv.G) * sv.batch * 256 <= kPrepWideMaxThreads;
   auto prep = wide ? replay_verify_prep_kernel<P, N, T, 256> : replay_verify_prep_kernel<P, N, T, 128>;
   const size_t psmem = static_cast<size_t>(sv.cap + kMaxDrafts) * N * sizeof(T);
-  if (psmem > 48 * 1024 &&
+  if (psmem > kSmemNoOptIn &&
       cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
@@ -484,7 +484,7 @@ static int launch(const StoreView& sv, int TT, const void* x, const void* B, con
     kern = replay_verify_tc_kernel<P, N, T>;
     smem = tc_verify_smem<P, N, T>(TT, sv.cap);
   }
-  if (smem > 48 * 1024 &&
+  if (smem > kSmemNoOptIn &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;

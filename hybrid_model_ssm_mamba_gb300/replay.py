@@ -21,7 +21,7 @@ __all__ = [
     "ReplayError", "ReplayConfig", "ReplayLayout", "load_library", "header_functions",
     "REPLAY_F32", "REPLAY_BF16", "REPLAY_RC_NONE", "REPLAY_RC_BF16", "REPLAY_RC_FP8E4M3", "REPLAY_RC_FP16",
     "REPLAY_RC_NVFP4",
-    "REPLAY_DEV_BAD_META", "REPLAY_DEV_BAD_ACCEPT",
+    "REPLAY_DEV_BAD_META", "REPLAY_DEV_BAD_ACCEPT", "REPLAY_DEV_COPY_TIMEOUT",
     "replay_layout_of", "replay_store_bytes", "replay_alloc", "replay_free", "replay_reset",
     "replay_load_state", "replay_export_state", "replay_step", "replay_verify",
     "replay_commit", "replay_flush", "replay_status", "conv_step", "conv_verify_snapshot",
@@ -32,7 +32,7 @@ HEADER = pathlib.Path(__file__).resolve().parent.parent / "include" / "replayssm
 
 REPLAY_F32, REPLAY_BF16 = 0, 1
 REPLAY_RC_NONE, REPLAY_RC_BF16, REPLAY_RC_FP8E4M3, REPLAY_RC_FP16, REPLAY_RC_NVFP4 = 0, 1, 2, 3, 4
-REPLAY_DEV_BAD_META, REPLAY_DEV_BAD_ACCEPT = 1, 2
+REPLAY_DEV_BAD_META, REPLAY_DEV_BAD_ACCEPT, REPLAY_DEV_COPY_TIMEOUT = 1, 2, 4
 REPLAY_STATIC_MAX_BATCH = 4096
 REPLAY_STATIC_MAX_COEFS = 1048576
 _ERRORS = {-1: "bad argument", -2: "unsupported shape or dtype", -3: "capacity exceeded",

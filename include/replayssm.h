@@ -91,6 +91,9 @@ extern "C" {
 /* device status bits (sticky until cleared by replay_status or replay_reset) */
 #define REPLAY_DEV_BAD_META 1    /* a sequence's ring metadata was out of range: its y is NaN */
 #define REPLAY_DEV_BAD_ACCEPT 2  /* commit with accept < 0 or > drafts pending: not applied */
+#define REPLAY_DEV_COPY_TIMEOUT 4 /* a step CTA's bulk copy of its checkpoint slab did not land
+                                     within its wait limit (1 s): that slab's y is NaN and its
+                                     ring and checkpoint are left as they were */
 
 typedef struct replay_config {
   int batch;        /* sequences */

@@ -25,10 +25,10 @@ def _cuda():
 
 
 def run_decode(shape, steps, L, seed=0, read_copy=R.REPLAY_RC_NONE, seqs=None, check_ckpt=True,
-               on_step=None):
+               on_step=None, T=0):
     """Decode `steps` tokens on the GPU and in the oracle (sequences `seqs`); returns the
     worst output error, the worst post-flush checkpoint error and the store."""
-    st, A, D = make_store(shape, seed, L=L, read_copy=read_copy)
+    st, A, D = make_store(shape, seed, L=L, T=T, read_copy=read_copy)
     sel = np.arange(shape.batch) if seqs is None else np.asarray(seqs)
     H, P, N = shape.nheads, shape.headdim, shape.dstate
     orc = Mamba2Decoder(A, D, shape.ngroups, np.zeros((len(sel), H, P, N)))
@@ -138,6 +138,55 @@ def test_longest_window(batch, heads, groups, dtype, read_copy):
     wy, wh, _, _ = run_decode(shape, 72, 64, seed=37, read_copy=read_copy, seqs=[0, batch - 1])
     bound = TOL if read_copy == R.REPLAY_RC_NONE else 1e-2
     assert wy <= bound and wh <= TOL, (wy, wh)
+
+
+@pytest.mark.parametrize("N,dtype,L,T", [
+    (128, "f32", 16, 0), (128, "bf16", 9, 2), (64, "f32", 3, 0), (64, "bf16", 24, 0),
+    (256, "f32", 13, 0), (256, "bf16", 1, 0)])
+def test_known_flush_on_the_large_call_path(N, dtype, L, T):
+    """A flush the host sees coming, on a call of more than 1024 slabs (the prep kernel and
+    the one-head-per-CTA kernel, which then loads the FP32 checkpoint before the prep wait):
+    every dstate, both input types, folds of 1 to 24 records, and a ring sized for verify
+    (T = 2). Outputs and checkpoints against the FP64 oracle at the FP32 bar."""
+    shape = sg.LayerShape(40, 32, 64, N, 4, dtype)
+    wy, wh, st, _ = run_decode(shape, 2 * L + 3, L, seed=41, seqs=[0, 17, 39], T=T)
+    assert st.layout.cap == (L + 2 * T - 1 if T else L)
+    assert wy <= TOL and wh <= TOL, (wy, wh)
+
+
+def test_wrong_phase_hint_still_follows_the_oracle():
+    """The host's count of buffered records only picks kernels; every kernel follows the
+    plan the device reads from the ring metadata. Here the device state is rewound behind
+    the host's back (regions restored after two extra steps), so the host expects a flush
+    where the ring holds one record (the flush kernel meets a non-flush plan), and later a
+    non-flush step where the ring is full (the bulk-copy read kernel meets a flush plan and
+    folds from the records in global memory). Outputs and checkpoints follow the oracle."""
+    shape = sg.LayerShape(40, 32, 64, 128, 4, "bf16")
+    L, seed, sel = 4, 43, np.array([0, 21, 39])
+    st, A, D = make_store(shape, seed, L=L)
+    orc = Mamba2Decoder(A, D, 4, np.zeros((3, 32, 64, 128)))
+    y = torch.empty(40, 32, 64, device="cuda")
+
+    def step(t):
+        devs, f64 = step_inputs(shape, seed, t, sel)
+        st.step(*devs, y)
+        return rel_vec_err(y[sel].cpu().numpy(), orc.step(*f64), 2).max()
+
+    assert step(0) <= TOL
+    names = ("h0", "meta", "xbuf", "bbuf", "dtbuf")
+    saved = {k: st.region(k).clone() for k in names}
+    for t in (100, 101):                             # steps the oracle does not see
+        devs, _ = step_inputs(shape, seed, t)
+        st.step(*devs, y)
+    for k in names:
+        st.region(k).copy_(saved[k])
+    for t in range(1, 8):                            # the device flushes after tokens 3 and 7
+        assert step(t) <= TOL, t
+        if t in (3, 7):
+            h0 = st.region("h0")[sel].cpu().numpy()
+            assert rel_vec_err(h0, orc.h, 2).max() <= TOL, t
+            assert np.all(st.region("meta").cpu().numpy()[:, 1] == 0)
+    assert st.status() == 0
 
 
 def test_verify_fullest_ring():
