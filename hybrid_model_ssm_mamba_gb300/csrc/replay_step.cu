@@ -261,18 +261,22 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
 // allows 4 such CTAs; loads into registers also pass through L1, which a shared-memory
 // carveout shrinks. Here one thread brings the slab into shared memory with one bulk copy
 // (neither registers nor L1 hold it in flight), the dot products stream from shared memory
-// row by row, and the few registers left let kReadCtas CTAs share an SM. A flush plan, not
-// expected here, folds a quarter of a warp's rows at a time with the records read from
-// global memory.
-template <int N>
-constexpr int kReadCtas = N >= 256 ? 3 : 6;
+// row by row, and the few registers left let kReadCtas CTAs share an SM.
+// FL: the launch is for a step the host knows flushes every sequence. The records are then
+// staged in shared memory past the slab while its copy lands, and the fold takes half of a
+// warp's rows at a time from shared memory (48 registers: 5 CTAs per SM, against 4 with a
+// register tile); the CTA also sends the slab of the CTA one wave later to L2. Without FL a
+// flush plan (not expected) folds a quarter of the rows at a time from the records in global
+// memory.
+template <int N, bool FL>
+constexpr int kReadCtas = N >= 256 ? (FL ? 2 : 3) : (FL ? 5 : 6);
 
-template <int P, int N, class T>
-__global__ void __launch_bounds__(kThreads, kReadCtas<N>)
+template <int P, int N, class T, bool FL>
+__global__ void __launch_bounds__(kThreads, kReadCtas<N, FL>)
 replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
                         const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
   using TL = Tile<P, N>;
-  constexpr int RPW = TL::RPW, E = TL::E, VEC = TL::VEC, NVEC = TL::NVEC, HR = RPW / 4;
+  constexpr int RPW = TL::RPW, E = TL::E, VEC = TL::VEC, NVEC = TL::NVEC, HR = FL ? RPW / 2 : RPW / 4;
   constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
   extern __shared__ float4 smem4[];
   __shared__ __align__(8) unsigned long long s_bar;
@@ -291,6 +295,7 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
     mbar_init(&s_bar);
     bulk_load(s_h, h0, P * N * sizeof(float), &s_bar);
   }
+  if (FL) prefetch_next_wave<P, N, REPLAY_RC_NONE>(sv, slab, 1, kReadCtas<N, FL>, true);
   float cv[E];
   load_cols<P, N>(C + bo, lane, cv);
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
@@ -303,10 +308,14 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   const float* cf = sv.coef + static_cast<size_t>(slab) * (cap + 1);
   const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
   auto x_of = [&](int s) { return s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P : x + xo; };
+  auto b_of = [&](int s) { return s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo; };
+  float* sm_u = s_h + P * N;     // FL: [k][P] w_s x_s, then [k][N] B_s
+  float* sm_b = sm_u + cap * P;
   float xr[RPW];
   if (pl.z == kPlanNonFlush) record_terms<RPW, T>(x_of, cf, k, warp, lane, xr);
+  if (FL && pl.z == kPlanFlush) stage_weighted<P, N, T>(x_of, b_of, cf, k, sm_u, sm_b);
   // The slab must have landed before it is read or the CTA exits; one thread waits, the rest
-  // at the barrier. A copy past its limit leaves this slab's y NaN and its state untouched
+  // at the barrier (which also publishes a flush's staging). A copy past its limit leaves this slab's y NaN and its state untouched
   // (after a second bounded wait).
   if (tid == 0) {
     const bool ok = mbar_wait(&s_bar, 0, kCopyWaitNs);
@@ -339,12 +348,11 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
     return;
   }
 
-  // flush: h <- Gamma h + sum_s w_s x_s B_s^T, a quarter of the warp's rows at a time
-  auto b_of = [&](int s) { return s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo; };
+  // flush: h <- Gamma h + sum_s w_s x_s B_s^T, HR of the warp's rows at a time
   const float gam = cf[cap];
   float part[RPW];
 #pragma unroll
-  for (int hf = 0; hf < 4; ++hf) {
+  for (int hf = 0; hf < RPW / HR; ++hf) {
     const int r0 = warp * RPW + hf * HR;
     float hv[HR][E];
 #pragma unroll
@@ -357,16 +365,21 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
         for (int e = 0; e < VEC; ++e) hv[i][v * VEC + e] = gam * t[e];
       }
     for (int s = 0; s < k; ++s) {
-      float bv[E];
-      load_cols<P, N>(b_of(s), lane, bv);
-      const T* xs = x_of(s) + r0;
-      const float w = cf[s];
+      float u[HR], bv[E];
+      if constexpr (FL) {
+        load_rows<HR>(sm_u + s * P + r0, u);
+        load_cols<P, N>(sm_b + s * N, lane, bv);
+      } else {
+        load_cols<P, N>(b_of(s), lane, bv);
+        const T* xs = x_of(s) + r0;
+        const float w = cf[s];
 #pragma unroll
-      for (int i = 0; i < HR; ++i) {
-        const float ui = w * to_f(xs[i]);
-#pragma unroll
-        for (int e = 0; e < E; ++e) hv[i][e] = fmaf(ui, bv[e], hv[i][e]);
+        for (int i = 0; i < HR; ++i) u[i] = w * to_f(xs[i]);
       }
+#pragma unroll
+      for (int i = 0; i < HR; ++i)
+#pragma unroll
+        for (int e = 0; e < E; ++e) hv[i][e] = fmaf(u[i], bv[e], hv[i][e]);
     }
 #pragma unroll
     for (int i = 0; i < HR; ++i) {
@@ -974,9 +987,13 @@ static int launch(const StoreView& sv, int all_n, const void* x, const void* B, 
                         stream, sv, tx, tB, tC, tdt, y);
   }
   if constexpr (RC == REPLAY_RC_NONE) {
-    if (all_n >= 0 && !all_flush)
-      return pdl_launch(replay_step_read_kernel<P, N, T>, dim3(sv.hpg, sv.G, sv.batch),
-                        static_cast<size_t>(P) * N * sizeof(float), stream, sv, tx, tB, tC, tdt, y);
+    const size_t slab_bytes = static_cast<size_t>(P) * N * sizeof(float);
+    if (all_flush)
+      return pdl_launch(replay_step_read_kernel<P, N, T, true>, dim3(sv.hpg, sv.G, sv.batch), slab_bytes + smem,
+                        stream, sv, tx, tB, tC, tdt, y);
+    if (all_n >= 0)
+      return pdl_launch(replay_step_read_kernel<P, N, T, false>, dim3(sv.hpg, sv.G, sv.batch), slab_bytes, stream,
+                        sv, tx, tB, tC, tdt, y);
   }
   return pdl_launch(replay_step_kernel<P, N, T, RC>, dim3(sv.hpg, sv.G, sv.batch), smem, stream, sv, tx, tB, tC,
                     tdt, y, all_flush ? 1 : 0);
