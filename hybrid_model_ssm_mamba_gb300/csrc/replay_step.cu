@@ -255,6 +255,170 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------------------
+// replay_step_copy_read_kernel: a bf16, E4M3 or FP16 read-copy step the host knows flushes
+// no sequence. The CTA's HPC copy slabs are contiguous, so one bulk copy brings them into
+// shared memory (the packed tiles no longer take 32 registers, and the copy is in flight
+// without holding registers or L1), and every head's record terms are loaded before the copy
+// is waited for, so the HPC heads' record latencies overlap the copy instead of following
+// one dot product after another. A flush plan, not expected here, is folded head by head
+// from the records in global memory.
+template <int N, int HPC>
+constexpr int kCopyReadCtas = N >= 256 ? 3 : (HPC >= 4 ? 4 : 6);
+
+template <int P, int N, class T, int RC, int HPC>
+__global__ void __launch_bounds__(kThreads, kCopyReadCtas<N, HPC>)
+replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
+                             const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
+  using TL = Tile<P, N>;
+  constexpr int RPW = TL::RPW, E = TL::E, VEC = TL::VEC, NVEC = TL::NVEC;
+  constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
+  constexpr int ESZ = RC == REPLAY_RC_FP8E4M3 ? 1 : 2;
+  constexpr unsigned SLAB_BYTES = P * N * ESZ;
+  using PT = typename PackOf<RC, VEC>::type;
+  extern __shared__ float4 smem4[];
+  __shared__ float s_red[kWarps];
+  __shared__ __align__(8) unsigned long long s_bar;
+  __shared__ int s_landed;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int hfirst = g * sv.hpg + blockIdx.x * HPC;
+  const int slab0 = b * sv.H + hfirst;
+  const int cap = sv.cap;
+  const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
+  const uint8_t* s_rc = reinterpret_cast<const uint8_t*>(smem4);
+  if (tid == 0) {
+    mbar_init(&s_bar);
+    bulk_load(smem4, static_cast<const uint8_t*>(sv.rc) + static_cast<size_t>(slab0) * SLAB_BYTES,
+              HPC * SLAB_BYTES, &s_bar);
+  }
+  auto tile_pack = [&](int hh, int i, int v) {
+    return *reinterpret_cast<const PT*>(
+        s_rc + (static_cast<size_t>(hh) * P * N + TL::row(warp, i) * N + TL::col(lane, v)) * ESZ);
+  };
+  float scl[HPC];
+#pragma unroll
+  for (int hh = 0; hh < HPC; ++hh) scl[hh] = RC == REPLAY_RC_FP8E4M3 ? sv.scale[slab0 + hh] : 1.f;
+  float cv[E];
+  load_cols<P, N>(C + bo, lane, cv);
+  const int myrow = warp * RPW + transpose_index<RPW>(lane);
+
+  griddep_wait();  // plan and coefficients of this step are written
+  const int4 pl = sv.plan[b];
+  const int start = pl.x, n = pl.y, k = n + 1;
+  auto x_of_head = [&](int hh, int s) {
+    const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, hfirst + hh, g);
+    return s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P
+                 : x + static_cast<size_t>(slab0 + hh) * P;
+  };
+  float ex[HPC][RPW];
+  if (pl.z == kPlanNonFlush) {
+#pragma unroll
+    for (int hh = 0; hh < HPC; ++hh) {
+      const float* cf = sv.coef + static_cast<size_t>(slab0 + hh) * (cap + 1);
+      record_terms<RPW, T>([&](int s) { return x_of_head(hh, s); }, cf, k, warp, lane, ex[hh]);
+    }
+  }
+  // The copy must have landed before it is read or the CTA exits (bounded wait, see the FP32
+  // read kernel).
+  if (tid == 0) {
+    const bool ok = mbar_wait(&s_bar, 0, kCopyWaitNs);
+    if (!ok) {
+      set_status(sv.status, REPLAY_DEV_COPY_TIMEOUT);
+      mbar_wait(&s_bar, 0, kCopyWaitNs);
+    }
+    s_landed = ok;
+  }
+  __syncthreads();
+  if (!s_landed || pl.z == kPlanBad) {
+    for (int hh = 0; hh < HPC; ++hh)
+      if (tid < P) y[static_cast<size_t>(slab0 + hh) * P + tid] = __int_as_float(0x7fc00000);
+    return;
+  }
+
+  if (pl.z == kPlanNonFlush) {
+    const int slot = ring_slot(start, n, cap);
+#pragma unroll
+    for (int hh = 0; hh < HPC; ++hh) {
+      const int h = hfirst + hh, slab = slab0 + hh;
+      const size_t xo = static_cast<size_t>(slab) * P;
+      const float gam = sv.coef[static_cast<size_t>(slab) * (cap + 1) + cap];
+      float part[RPW];
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        float hc = 0.f;
+#pragma unroll
+        for (int v = 0; v < NVEC; ++v) {
+          float w[VEC];
+          unpack<RC, VEC>(tile_pack(hh, i, v), scl[hh], w);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) hc = fmaf(w[e], cv[v * VEC + e], hc);
+        }
+        part[i] = fmaf(gam, hc, ex[hh][i]);
+      }
+      const float sum = warp_transpose_reduce<RPW>(part, lane);
+      if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
+      const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+      if (tid < XC) {
+        *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
+            *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
+      } else if (blockIdx.x == 0 && hh == 0 && tid < XC + BC) {
+        const int c = tid - XC;
+        *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+            *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+      } else if (tid == XC + BC) {
+        ring.dt[slot] = dt[slab];
+      }
+    }
+    return;
+  }
+
+  // flush (not expected): head by head, from the FP32 checkpoint (or from the copy when the
+  // copy is the checkpoint), records read from global memory
+  for (int hh = 0; hh < HPC; ++hh) {
+    const int h = hfirst + hh, slab = slab0 + hh;
+    const size_t xo = static_cast<size_t>(slab) * P;
+    const float* cf = sv.coef + static_cast<size_t>(slab) * (cap + 1);
+    const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+    float hv[RPW][E];
+    if (sv.shared) {
+#pragma unroll
+      for (int i = 0; i < RPW; ++i)
+#pragma unroll
+        for (int v = 0; v < NVEC; ++v) {
+          float w[VEC];
+          unpack<RC, VEC>(tile_pack(hh, i, v), scl[hh], w);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) hv[i][v * VEC + e] = w[e];
+        }
+    } else {
+      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    }
+    const float gam = cf[cap];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+#pragma unroll
+      for (int e = 0; e < E; ++e) hv[i][e] *= gam;
+    for (int s = 0; s < k; ++s) {
+      float u[RPW], bv[E];
+      load_rows<RPW>(x_of_head(hh, s) + warp * RPW, u);
+      load_cols<P, N>(s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo, lane, bv);
+      const float w = cf[s];
+#pragma unroll
+      for (int i = 0; i < RPW; ++i)
+#pragma unroll
+        for (int e = 0; e < E; ++e) hv[i][e] = fmaf(w * u[i], bv[e], hv[i][e]);
+    }
+    float zero[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) zero[i] = 0.f;
+    const float sum = tile_rows_dot<P, N>(hv, cv, 1.f, zero, lane);
+    if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
+    write_checkpoint<P, N, RC>(sv, slab, s_red, hv, pl.w);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // replay_step_read_kernel: the FP32-checkpoint step when the host knows that no sequence
 // flushes (the non-flush steps of a window). Such a step only reads, so its speed is the
 // bytes an SM keeps in flight. A register tile holds 32 KB per CTA and the register file
@@ -982,6 +1146,10 @@ static int launch(const StoreView& sv, int all_n, const void* x, const void* B, 
                         sv, tx, tB, tC, tdt, y);
   } else if constexpr (RC != REPLAY_RC_NONE && RC != REPLAY_RC_NVFP4) {
     constexpr int HPC = heads_per_cta<N, RC>();
+    constexpr size_t kCopyBytes = static_cast<size_t>(HPC) * P * N * (RC == REPLAY_RC_FP8E4M3 ? 1 : 2);
+    if (all_n >= 0 && !all_flush && HPC > 1 && sv.hpg % HPC == 0)
+      return pdl_launch(replay_step_copy_read_kernel<P, N, T, RC, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch),
+                        kCopyBytes, stream, sv, tx, tB, tC, tdt, y);
     if (!all_flush && HPC > 1 && sv.hpg % HPC == 0)
       return pdl_launch(replay_step_copy_kernel<P, N, T, RC, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch), smem,
                         stream, sv, tx, tB, tC, tdt, y);

@@ -145,7 +145,8 @@ def test_longest_window(batch, heads, groups, dtype, read_copy):
     (256, "f32", 13, 0), (256, "bf16", 1, 0)])
 def test_known_flush_on_the_large_call_path(N, dtype, L, T):
     """A flush the host sees coming, on a call of more than 1024 slabs (the prep kernel and
-    the one-head-per-CTA kernel, which then loads the FP32 checkpoint before the prep wait):
+    the flush instantiation of the bulk-copy read kernel: records staged while the slab
+    lands, fold from shared memory):
     every dstate, both input types, folds of 1 to 24 records, and a ring sized for verify
     (T = 2). Outputs and checkpoints against the FP64 oracle at the FP32 bar."""
     shape = sg.LayerShape(40, 32, 64, N, 4, dtype)
@@ -154,26 +155,31 @@ def test_known_flush_on_the_large_call_path(N, dtype, L, T):
     assert wy <= TOL and wh <= TOL, (wy, wh)
 
 
-def test_wrong_phase_hint_still_follows_the_oracle():
+@pytest.mark.parametrize("rc,bound", [(R.REPLAY_RC_NONE, TOL), (R.REPLAY_RC_BF16, 1e-2),
+                                      (R.REPLAY_RC_FP8E4M3, 0.25)])
+def test_wrong_phase_hint_still_follows_the_oracle(rc, bound):
     """The host's count of buffered records only picks kernels; every kernel follows the
     plan the device reads from the ring metadata. Here the device state is rewound behind
     the host's back (regions restored after two extra steps), so the host expects a flush
     where the ring holds one record (the flush kernel meets a non-flush plan), and later a
-    non-flush step where the ring is full (the bulk-copy read kernel meets a flush plan and
-    folds from the records in global memory). Outputs and checkpoints follow the oracle."""
+    non-flush step where the ring is full (the bulk-copy read kernel, FP32 or read copy,
+    meets a flush plan and folds from the records in global memory). Non-flush outputs read
+    the copy (its bound); flush outputs and checkpoints follow the oracle at 1e-4."""
     shape = sg.LayerShape(40, 32, 64, 128, 4, "bf16")
     L, seed, sel = 4, 43, np.array([0, 21, 39])
-    st, A, D = make_store(shape, seed, L=L)
+    st, A, D = make_store(shape, seed, L=L, read_copy=rc)
     orc = Mamba2Decoder(A, D, 4, np.zeros((3, 32, 64, 128)))
     y = torch.empty(40, 32, 64, device="cuda")
 
     def step(t):
         devs, f64 = step_inputs(shape, seed, t, sel)
         st.step(*devs, y)
-        return rel_vec_err(y[sel].cpu().numpy(), orc.step(*f64), 2).max()
+        err = rel_vec_err(y[sel].cpu().numpy(), orc.step(*f64), 2).max()
+        return err <= (TOL if t in (3, 7) else bound)
 
-    assert step(0) <= TOL
-    names = ("h0", "meta", "xbuf", "bbuf", "dtbuf")
+    assert step(0)
+    names = ("h0", "meta", "xbuf", "bbuf", "dtbuf") + (("rc",) if rc else ()) + \
+        (("scale",) if rc == R.REPLAY_RC_FP8E4M3 else ())
     saved = {k: st.region(k).clone() for k in names}
     for t in (100, 101):                             # steps the oracle does not see
         devs, _ = step_inputs(shape, seed, t)
@@ -181,7 +187,7 @@ def test_wrong_phase_hint_still_follows_the_oracle():
     for k in names:
         st.region(k).copy_(saved[k])
     for t in range(1, 8):                            # the device flushes after tokens 3 and 7
-        assert step(t) <= TOL, t
+        assert step(t), t
         if t in (3, 7):
             h0 = st.region("h0")[sel].cpu().numpy()
             assert rel_vec_err(h0, orc.h, 2).max() <= TOL, t
