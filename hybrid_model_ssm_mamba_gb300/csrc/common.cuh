@@ -251,6 +251,32 @@ __device__ __forceinline__ void unpack(typename PackOf<RC, VEC>::type v, float s
   }
 }
 
+// The same VEC values as VEC / 2 pairs for packed FP32 arithmetic, without the E4M3 slab
+// scale (a caller applies it once to a sum). bf16 widens by shifts: a bf16 is the top half of
+// an FP32.
+template <int RC, int VEC>
+__device__ __forceinline__ void unpack_pairs(typename PackOf<RC, VEC>::type v, float2 (&o)[VEC / 2]) {
+  unsigned w[VEC / 2];
+  if constexpr (sizeof(v) == 8) {
+    w[0] = v.x;
+    w[1] = v.y;
+  } else if constexpr (VEC == 4) {
+    w[0] = v & 0xffffu;  // E4M3: two codes per pair
+    w[1] = v >> 16;
+  } else {
+    w[0] = v;
+  }
+#pragma unroll
+  for (int j = 0; j < VEC / 2; ++j) {
+    if constexpr (RC == REPLAY_RC_BF16)
+      o[j] = make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xffff0000u));
+    else if constexpr (RC == REPLAY_RC_FP16)
+      o[j] = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+    else
+      o[j] = e4m3x2_to_float2(static_cast<unsigned short>(w[j]));
+  }
+}
+
 // ------------------------------------------------------------------ slab register tile
 // A P x N slab is spread over 8 warps: warp w owns rows w*RPW .. w*RPW+RPW-1; in each row a
 // lane owns NVEC vectors of VEC columns, vector v at column v*32*VEC + lane*VEC. Every

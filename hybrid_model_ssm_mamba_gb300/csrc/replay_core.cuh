@@ -207,15 +207,16 @@ __device__ __forceinline__ float smem_rows_dot(const float* slab, const float (&
   float part[TL::RPW];
 #pragma unroll
   for (int i = 0; i < TL::RPW; ++i) {
-    float hc = 0.f;
+    float2 hc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int v = 0; v < TL::NVEC; ++v) {
       float t[TL::VEC];
       ldv<TL::VEC>(slab + TL::row(warp, i) * N + TL::col(lane, v), t);
 #pragma unroll
-      for (int e = 0; e < TL::VEC; ++e) hc = fmaf(t[e], cv[v * TL::VEC + e], hc);
+      for (int e = 0; e < TL::VEC; e += 2)
+        hc = __ffma2_rn(make_float2(t[e], t[e + 1]), make_float2(cv[v * TL::VEC + e], cv[v * TL::VEC + e + 1]), hc);
     }
-    part[i] = fmaf(gam, hc, extra[i]);
+    part[i] = fmaf(gam, hc.x + hc.y, extra[i]);
   }
   return warp_transpose_reduce<TL::RPW>(part, lane);
 }
@@ -322,7 +323,12 @@ __device__ __forceinline__ void fold_tile(const RingImage<T>& im, SlotOf slot_of
 #pragma unroll
     for (int i = 0; i < TL::RPW; ++i)
 #pragma unroll
-      for (int e = 0; e < TL::E; ++e) hv[i][e] = fmaf(u[i], bv[e], hv[i][e]);
+      for (int e = 0; e < TL::E; e += 2) {  // packed FP32 FMAs, two columns at a time
+        const float2 r = __ffma2_rn(make_float2(u[i], u[i]), make_float2(bv[e], bv[e + 1]),
+                                    make_float2(hv[i][e], hv[i][e + 1]));
+        hv[i][e] = r.x;
+        hv[i][e + 1] = r.y;
+      }
   }
 }
 
@@ -384,7 +390,12 @@ __device__ __forceinline__ void fold_staged(const float* sm_u, const float* sm_b
 #pragma unroll
     for (int i = 0; i < TL::RPW; ++i)
 #pragma unroll
-      for (int e = 0; e < TL::E; ++e) hv[i][e] = fmaf(u[i], bv[e], hv[i][e]);
+      for (int e = 0; e < TL::E; e += 2) {  // packed FP32 FMAs, two columns at a time
+        const float2 r = __ffma2_rn(make_float2(u[i], u[i]), make_float2(bv[e], bv[e + 1]),
+                                    make_float2(hv[i][e], hv[i][e + 1]));
+        hv[i][e] = r.x;
+        hv[i][e + 1] = r.y;
+      }
   }
 }
 

@@ -262,6 +262,72 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
 // is waited for, so the HPC heads' record latencies overlap the copy instead of following
 // one dot product after another. A flush plan, not expected here, is folded head by head
 // from the records in global memory.
+// The flush of a read-copy CTA's HPC heads when a flush plan reaches the bulk-copy read
+// kernel (the host expected none): head by head, from the FP32 checkpoint (or from the copy
+// in shared memory when the copy is the checkpoint), records read from global memory. Kept
+// out of line: it holds a whole register tile, the read path does not.
+template <int P, int N, class T, int RC, int HPC>
+__device__ __noinline__ void copy_read_flush(const StoreView& sv, const T* __restrict__ x, const T* __restrict__ B,
+                                             const T* __restrict__ C, float* __restrict__ y, const uint8_t* s_rc,
+                                             const float* scl, int start, int n, int epoch, float* s_red) {
+  using TL = Tile<P, N>;
+  constexpr int RPW = TL::RPW, E = TL::E, VEC = TL::VEC, NVEC = TL::NVEC;
+  constexpr int ESZ = RC == REPLAY_RC_FP8E4M3 ? 1 : 2;
+  using PT = typename PackOf<RC, VEC>::type;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int hfirst = g * sv.hpg + blockIdx.x * HPC;
+  const int slab0 = b * sv.H + hfirst;
+  const int cap = sv.cap, k = n + 1;
+  const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
+  const int myrow = warp * RPW + transpose_index<RPW>(lane);
+  float cv[E];
+  load_cols<P, N>(C + bo, lane, cv);
+  for (int hh = 0; hh < HPC; ++hh) {
+    const int h = hfirst + hh, slab = slab0 + hh;
+    const size_t xo = static_cast<size_t>(slab) * P;
+    const float* cf = sv.coef + static_cast<size_t>(slab) * (cap + 1);
+    const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+    float hv[RPW][E];
+    if (sv.shared) {
+#pragma unroll
+      for (int i = 0; i < RPW; ++i)
+#pragma unroll
+        for (int v = 0; v < NVEC; ++v) {
+          const size_t elem = static_cast<size_t>(hh) * P * N + TL::row(warp, i) * N + TL::col(lane, v);
+          float w[VEC];
+          unpack<RC, VEC>(*reinterpret_cast<const PT*>(s_rc + elem * ESZ), scl[hh], w);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) hv[i][v * VEC + e] = w[e];
+        }
+    } else {
+      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    }
+    const float gam = cf[cap];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+#pragma unroll
+      for (int e = 0; e < E; ++e) hv[i][e] *= gam;
+    for (int s = 0; s < k; ++s) {
+      const int slot = ring_slot(start, s, cap);
+      float u[RPW], bv[E];
+      load_rows<RPW>((s < n ? ring.x + static_cast<size_t>(slot) * P : x + xo) + warp * RPW, u);
+      load_cols<P, N>(s < n ? ring.b + static_cast<size_t>(slot) * N : B + bo, lane, bv);
+      const float w = cf[s];
+#pragma unroll
+      for (int i = 0; i < RPW; ++i)
+#pragma unroll
+        for (int e = 0; e < E; ++e) hv[i][e] = fmaf(w * u[i], bv[e], hv[i][e]);
+    }
+    float zero[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) zero[i] = 0.f;
+    const float sum = tile_rows_dot<P, N>(hv, cv, 1.f, zero, lane);
+    if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
+    write_checkpoint<P, N, RC>(sv, slab, s_red, hv, epoch);
+  }
+}
+
 template <int N, int HPC>
 constexpr int kCopyReadCtas = N >= 256 ? 3 : (HPC >= 4 ? 4 : 6);
 
@@ -292,15 +358,18 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
     bulk_load(smem4, static_cast<const uint8_t*>(sv.rc) + static_cast<size_t>(slab0) * SLAB_BYTES,
               HPC * SLAB_BYTES, &s_bar);
   }
+  const uint8_t* my_rc = s_rc + (TL::row(warp, 0) * N + TL::col(lane, 0)) * ESZ;  // this lane's first pack
   auto tile_pack = [&](int hh, int i, int v) {
-    return *reinterpret_cast<const PT*>(
-        s_rc + (static_cast<size_t>(hh) * P * N + TL::row(warp, i) * N + TL::col(lane, v)) * ESZ);
+    return *reinterpret_cast<const PT*>(my_rc + (hh * P * N + i * N + v * 32 * VEC) * ESZ);
   };
   float scl[HPC];
 #pragma unroll
   for (int hh = 0; hh < HPC; ++hh) scl[hh] = RC == REPLAY_RC_FP8E4M3 ? sv.scale[slab0 + hh] : 1.f;
   float cv[E];
   load_cols<P, N>(C + bo, lane, cv);
+  float2 cv2[E / 2];
+#pragma unroll
+  for (int j = 0; j < E / 2; ++j) cv2[j] = make_float2(cv[2 * j], cv[2 * j + 1]);
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
 
   griddep_wait();  // plan and coefficients of this step are written
@@ -342,19 +411,20 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
     for (int hh = 0; hh < HPC; ++hh) {
       const int h = hfirst + hh, slab = slab0 + hh;
       const size_t xo = static_cast<size_t>(slab) * P;
-      const float gam = sv.coef[static_cast<size_t>(slab) * (cap + 1) + cap];
+      // Gamma h . C with the copy's pairs on packed FP32 FMAs; the slab scale once per row
+      const float gs = sv.coef[static_cast<size_t>(slab) * (cap + 1) + cap] * scl[hh];
       float part[RPW];
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
-        float hc = 0.f;
+        float2 hc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int v = 0; v < NVEC; ++v) {
-          float w[VEC];
-          unpack<RC, VEC>(tile_pack(hh, i, v), scl[hh], w);
+          float2 w[VEC / 2];
+          unpack_pairs<RC, VEC>(tile_pack(hh, i, v), w);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) hc = fmaf(w[e], cv[v * VEC + e], hc);
+          for (int j = 0; j < VEC / 2; ++j) hc = __ffma2_rn(w[j], cv2[v * VEC / 2 + j], hc);
         }
-        part[i] = fmaf(gam, hc, ex[hh][i]);
+        part[i] = fmaf(gs, hc.x + hc.y, ex[hh][i]);
       }
       const float sum = warp_transpose_reduce<RPW>(part, lane);
       if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
@@ -373,49 +443,8 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
     return;
   }
 
-  // flush (not expected): head by head, from the FP32 checkpoint (or from the copy when the
-  // copy is the checkpoint), records read from global memory
-  for (int hh = 0; hh < HPC; ++hh) {
-    const int h = hfirst + hh, slab = slab0 + hh;
-    const size_t xo = static_cast<size_t>(slab) * P;
-    const float* cf = sv.coef + static_cast<size_t>(slab) * (cap + 1);
-    const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
-    float hv[RPW][E];
-    if (sv.shared) {
-#pragma unroll
-      for (int i = 0; i < RPW; ++i)
-#pragma unroll
-        for (int v = 0; v < NVEC; ++v) {
-          float w[VEC];
-          unpack<RC, VEC>(tile_pack(hh, i, v), scl[hh], w);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) hv[i][v * VEC + e] = w[e];
-        }
-    } else {
-      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
-    }
-    const float gam = cf[cap];
-#pragma unroll
-    for (int i = 0; i < RPW; ++i)
-#pragma unroll
-      for (int e = 0; e < E; ++e) hv[i][e] *= gam;
-    for (int s = 0; s < k; ++s) {
-      float u[RPW], bv[E];
-      load_rows<RPW>(x_of_head(hh, s) + warp * RPW, u);
-      load_cols<P, N>(s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo, lane, bv);
-      const float w = cf[s];
-#pragma unroll
-      for (int i = 0; i < RPW; ++i)
-#pragma unroll
-        for (int e = 0; e < E; ++e) hv[i][e] = fmaf(w * u[i], bv[e], hv[i][e]);
-    }
-    float zero[RPW];
-#pragma unroll
-    for (int i = 0; i < RPW; ++i) zero[i] = 0.f;
-    const float sum = tile_rows_dot<P, N>(hv, cv, 1.f, zero, lane);
-    if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
-    write_checkpoint<P, N, RC>(sv, slab, s_red, hv, pl.w);
-  }
+  // flush (not expected): out of line, so that its registers do not weigh on the read path
+  copy_read_flush<P, N, T, RC, HPC>(sv, x, B, C, y, s_rc, scl, start, n, pl.w, s_red);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -543,7 +572,12 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
 #pragma unroll
       for (int i = 0; i < HR; ++i)
 #pragma unroll
-        for (int e = 0; e < E; ++e) hv[i][e] = fmaf(u[i], bv[e], hv[i][e]);
+        for (int e = 0; e < E; e += 2) {  // packed FP32 FMAs, two columns at a time
+          const float2 r = __ffma2_rn(make_float2(u[i], u[i]), make_float2(bv[e], bv[e + 1]),
+                                      make_float2(hv[i][e], hv[i][e + 1]));
+          hv[i][e] = r.x;
+          hv[i][e + 1] = r.y;
+        }
     }
 #pragma unroll
     for (int i = 0; i < HR; ++i) {
