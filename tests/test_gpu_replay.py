@@ -156,15 +156,15 @@ def test_known_flush_on_the_large_call_path(N, dtype, L, T):
 
 
 @pytest.mark.parametrize("rc,bound", [(R.REPLAY_RC_NONE, TOL), (R.REPLAY_RC_BF16, 1e-2),
-                                      (R.REPLAY_RC_FP8E4M3, 0.25)])
+                                      (R.REPLAY_RC_FP8E4M3, 0.25), (R.REPLAY_RC_NVFP4, 0.25)])
 def test_wrong_phase_hint_still_follows_the_oracle(rc, bound):
     """The host's count of buffered records only picks kernels; every kernel follows the
     plan the device reads from the ring metadata. Here the device state is rewound behind
     the host's back (regions restored after two extra steps), so the host expects a flush
     where the ring holds one record (the flush kernel meets a non-flush plan), and later a
-    non-flush step where the ring is full (the bulk-copy read kernel, FP32 or read copy,
-    meets a flush plan and folds from the records in global memory). Non-flush outputs read
-    the copy (its bound); flush outputs and checkpoints follow the oracle at 1e-4."""
+    non-flush step where the ring is full (the bulk-copy read kernels, FP32 or read copy, and
+    the NVFP4 kernel meet a flush plan). Non-flush outputs read the copy (its bound); flush
+    outputs and checkpoints follow the oracle at 1e-4."""
     shape = sg.LayerShape(40, 32, 64, 128, 4, "bf16")
     L, seed, sel = 4, 43, np.array([0, 21, 39])
     st, A, D = make_store(shape, seed, L=L, read_copy=rc)
@@ -179,7 +179,8 @@ def test_wrong_phase_hint_still_follows_the_oracle(rc, bound):
 
     assert step(0)
     names = ("h0", "meta", "xbuf", "bbuf", "dtbuf") + (("rc",) if rc else ()) + \
-        (("scale",) if rc == R.REPLAY_RC_FP8E4M3 else ())
+        (("scale",) if rc in (R.REPLAY_RC_FP8E4M3, R.REPLAY_RC_NVFP4) else ()) + \
+        (("bscale",) if rc == R.REPLAY_RC_NVFP4 else ())
     saved = {k: st.region(k).clone() for k in names}
     for t in (100, 101):                             # steps the oracle does not see
         devs, _ = step_inputs(shape, seed, t)
