@@ -1180,9 +1180,12 @@ static int launch(const StoreView& sv, int all_n, const void* x, const void* B, 
                         sv, tx, tB, tC, tdt, y);
   } else if constexpr (RC != REPLAY_RC_NONE && RC != REPLAY_RC_NVFP4) {
     constexpr int HPC = heads_per_cta<N, RC>();
-    constexpr size_t kCopyBytes = static_cast<size_t>(HPC) * P * N * (RC == REPLAY_RC_FP8E4M3 ? 1 : 2);
-    if (all_n >= 0 && !all_flush && HPC > 1 && sv.hpg % HPC == 0)
-      return pdl_launch(replay_step_copy_read_kernel<P, N, T, RC, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch),
+    // the bulk-copy kernel takes at most 2 heads of E4M3 at dstate 128 (16 KB): 6 CTAs per SM
+    // beat 4 with 4 heads each (measured)
+    constexpr int HR = RC == REPLAY_RC_FP8E4M3 && HPC == 4 && N == 128 ? 2 : HPC;
+    constexpr size_t kCopyBytes = static_cast<size_t>(HR) * P * N * (RC == REPLAY_RC_FP8E4M3 ? 1 : 2);
+    if (all_n >= 0 && !all_flush && HR > 1 && sv.hpg % HR == 0)
+      return pdl_launch(replay_step_copy_read_kernel<P, N, T, RC, HR>, dim3(sv.hpg / HR, sv.G, sv.batch),
                         kCopyBytes, stream, sv, tx, tB, tC, tdt, y);
     if (!all_flush && HPC > 1 && sv.hpg % HPC == 0)
       return pdl_launch(replay_step_copy_kernel<P, N, T, RC, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch), smem,
