@@ -180,7 +180,10 @@ int replay_export_state(replay_store* st, float* h_out, void* stream);
  *    h0, which is written once (and cast into the read copy, if any); y is read from the
  *    new FP32 checkpoint; the ring is emptied.
  * Non-flush steps read the read copy when one is configured; flushes always start from
- * the FP32 checkpoint ("Benefit 3"). Drafts pending from a verify are dropped. */
+ * the FP32 checkpoint ("Benefit 3"). Drafts pending from a verify are dropped. A sequence
+ * with out-of-range ring metadata gets NaN outputs and REPLAY_DEV_BAD_META; a CTA whose bulk
+ * copy of its state does not land within 1 s gives its slabs NaN outputs, leaves their state
+ * unchanged and sets REPLAY_DEV_COPY_TIMEOUT (read with replay_status). */
 int replay_step(replay_store* st, const void* x, const void* B, const void* C,
                 const void* dt, float* y, void* stream);
 
