@@ -488,14 +488,21 @@ def _decoded_copy(st, rc, h32):
     return out
 
 
-@pytest.mark.parametrize("rc", [R.REPLAY_RC_BF16, R.REPLAY_RC_FP16, R.REPLAY_RC_FP8E4M3])
-@pytest.mark.parametrize("batch,heads,groups,dtype", [(4, 8, 2, "f32"), (72, 128, 8, "bf16")])
-def test_copy_reads_follow_the_decoded_copy(rc, batch, heads, groups, dtype):
+_BF, _F16, _E4 = R.REPLAY_RC_BF16, R.REPLAY_RC_FP16, R.REPLAY_RC_FP8E4M3
+
+
+@pytest.mark.parametrize("rc,batch,heads,groups,dtype,dstate", [
+    (_BF, 4, 8, 2, "f32", 128), (_F16, 4, 8, 2, "f32", 128), (_E4, 4, 8, 2, "f32", 128),
+    (_BF, 72, 128, 8, "bf16", 128), (_F16, 72, 128, 8, "bf16", 128), (_E4, 72, 128, 8, "bf16", 128),
+    (_BF, 40, 32, 4, "bf16", 64), (_F16, 40, 32, 4, "f32", 64), (_E4, 40, 32, 4, "bf16", 64),
+    (_BF, 40, 32, 4, "f32", 256), (_E4, 40, 32, 4, "bf16", 256)])
+def test_copy_reads_follow_the_decoded_copy(rc, batch, heads, groups, dtype, dstate):
     """Non-flush outputs against the unrolled window evaluated in FP64 from the copy's own
     values (the format's decoding of the loaded FP32 state), within 1e-4: the copy is read
-    exactly, whichever kernel reads it (the fused small-call kernel; on the large call the
-    tensor-core kernel for bf16 and FP16, the several-heads kernel for E4M3)."""
-    shape = sg.LayerShape(batch, heads, 64, 128, groups, dtype)
+    exactly, whichever kernel reads it. Small calls take the fused kernel; calls of more than
+    1024 slabs take the bulk-copy several-heads kernel (2 heads per CTA at dstate 128, 4 at
+    64, 2 for E4M3 at 256) or, for a bf16 copy at dstate 256, the one-head-per-CTA kernel."""
+    shape = sg.LayerShape(batch, heads, 64, dstate, groups, dtype)
     L, seed = 8, 31
     st, A, D = make_store(shape, seed, L=L, read_copy=rc)
     sel = np.array([0, batch - 1])
