@@ -1,6 +1,7 @@
 // The C ABI of the library: argument checks on the host, the workspace layout, and
 // dispatch to the kernel launchers. Declarations and the meaning of every call are in
 // include/replayssm.h.
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <new>
@@ -91,8 +92,8 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   L.meta = take(Bn * 16);
   L.arrive = take(Bn * 4);
   L.status = take(4);
-  L.plan = take(Bn * 16);
-  L.coef = take(Bn * H * (static_cast<size_t>(c->max_draft_T) + 1) * (cap + 1) * 4);
+  L.plan = take(2 * Bn * 16);  // two: a step's plan is written while the previous step reads its own
+  L.coef = take(Bn * H * std::max<size_t>(static_cast<size_t>(c->max_draft_T) + 1, 2) * (cap + 1) * 4);
   L.total = off;
   *out = L;
   return REPLAY_OK;
@@ -118,6 +119,8 @@ int replay_alloc(const replay_config* c, void* workspace, size_t workspace_bytes
   if (st == nullptr) return REPLAY_ECAPACITY;
   st->cfg = *c;
   st->lay = L;
+  st->step_parity = 0;
+  st->prev_nonflush = 0;
   st->ws = static_cast<char*>(workspace);
   rssm::StoreView& sv = st->sv;
   sv.h0 = reinterpret_cast<float*>(st->ws + L.h0);
@@ -173,6 +176,7 @@ int replay_reset(replay_store* st, const int* seq_mask, void* stream) {
   }
   const int rc = rssm::launch_load(st->sv, st->sh, nullptr, seq_mask, as_stream(stream));
   st->all_n = rc == REPLAY_OK && seq_mask == nullptr ? 0 : -1;
+  st->prev_nonflush = 0;
   return rc;
 }
 
@@ -180,11 +184,13 @@ int replay_load_state(replay_store* st, const float* h, void* stream) {
   if (st == nullptr || h == nullptr) return REPLAY_EBADARG;
   const int rc = rssm::launch_load(st->sv, st->sh, h, nullptr, as_stream(stream));
   st->all_n = rc == REPLAY_OK ? 0 : -1;
+  st->prev_nonflush = 0;
   return rc;
 }
 
 int replay_export_state(replay_store* st, float* h_out, void* stream) {
   if (st == nullptr || h_out == nullptr) return REPLAY_EBADARG;
+  st->prev_nonflush = 0;
   return rssm::launch_fold(st->sv, st->sh, 1, h_out, as_stream(stream));
 }
 
@@ -193,8 +199,14 @@ int replay_step(replay_store* st, const void* x, const void* B, const void* C, c
   if (st == nullptr || x == nullptr || B == nullptr || C == nullptr || dt == nullptr || y == nullptr)
     return REPLAY_EBADARG;
   if (!aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
-  const int rc = rssm::launch_step(st->sv, st->sh, st->all_n, x, B, C, dt, y, as_stream(stream));
-  if (rc == REPLAY_OK) st->all_n = advance_all_n(st);
+  const int all_n = st->all_n;
+  const int rc = rssm::launch_step(st->sv, st->sh, all_n, st->step_parity, st->prev_nonflush, x, B, C, dt, y,
+                                   as_stream(stream));
+  st->prev_nonflush = rc == REPLAY_OK && all_n >= 0 && all_n + 1 < st->cfg.window_L && rssm::step_runs_prep(st->sv);
+  if (rc == REPLAY_OK) {
+    st->all_n = advance_all_n(st);
+    st->step_parity ^= 1;
+  }
   return rc;
 }
 
@@ -205,17 +217,20 @@ int replay_verify(replay_store* st, int T, const void* x, const void* B, const v
   if (T < 1 || !aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
   if (T > st->cfg.max_draft_T) return REPLAY_ECAPACITY;
   st->all_n = -1;
+  st->prev_nonflush = 0;
   return rssm::launch_verify(st->sv, st->sh, T, x, B, C, dt, y, as_stream(stream));
 }
 
 int replay_commit(replay_store* st, const int* accept, void* stream) {
   if (st == nullptr || accept == nullptr) return REPLAY_EBADARG;
   st->all_n = -1;
+  st->prev_nonflush = 0;
   return rssm::launch_commit(st->sv, accept, as_stream(stream));
 }
 
 int replay_flush(replay_store* st, void* stream) {
   if (st == nullptr) return REPLAY_EBADARG;
+  st->prev_nonflush = 0;
   const int rc = rssm::launch_fold(st->sv, st->sh, 0, nullptr, as_stream(stream));
   if (rc == REPLAY_OK) st->all_n = 0;
   return rc;

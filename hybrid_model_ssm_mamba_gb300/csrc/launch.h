@@ -31,8 +31,16 @@ struct Shape {
 
 // all_n: the ring count all sequences share before the step if the host knows it, else -1
 // (a kernel-choice hint only).
-int launch_step(const StoreView& sv, const Shape& sh, int all_n, const void* x, const void* B, const void* C,
-                const void* dt, float* y, cudaStream_t stream);
+// parity: which of the two plan and coefficient buffers this step uses (consecutive steps
+// alternate). overlap: the previous call on the stream was a step known to flush no sequence
+// that ran through the prep kernel; this step's prep may then start while that step's
+// per-head kernel still runs.
+int launch_step(const StoreView& sv, const Shape& sh, int all_n, int parity, int overlap, const void* x,
+                const void* B, const void* C, const void* dt, float* y, cudaStream_t stream);
+
+// Calls with at most this many (sequence, head) slabs take the fused step kernel (no prep).
+constexpr long long kFusedMaxSlabs = 1024;
+inline bool step_runs_prep(const StoreView& sv) { return static_cast<long long>(sv.batch) * sv.H > kFusedMaxSlabs; }
 int launch_verify(const StoreView& sv, const Shape& sh, int T, const void* x, const void* B,
                   const void* C, const void* dt, float* y, cudaStream_t stream);
 int launch_commit(const StoreView& sv, const int* accept, cudaStream_t stream);

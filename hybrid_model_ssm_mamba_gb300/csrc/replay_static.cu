@@ -75,7 +75,10 @@ extern "C" int replay_step_static_scratch(replay_store* st, const void* x, const
   sv.arrive = reinterpret_cast<int*>(scratch);
   sv.plan = reinterpret_cast<int4*>(scratch + kArriveBytes);
   sv.coef = reinterpret_cast<float*>(scratch + kArriveBytes + kPlanBytes);
-  rc = rssm::launch_step(sv, st->sh, st->all_n, x, B, C, dt, y, s);
+  // (one plan and coefficient buffer, and no overlap with the previous step: the memset
+  // above already separates the two)
+  rc = rssm::launch_step(sv, st->sh, st->all_n, 0, 0, x, B, C, dt, y, s);
+  st->prev_nonflush = 0;
   if (rc == REPLAY_OK) st->all_n = advance_all_n(st);
   return rc;
 }

@@ -35,7 +35,7 @@ constexpr int kPrepThreads = 128, kPrepWarps = kPrepThreads / 32;
 template <int P, int N, class T>
 __global__ void __launch_bounds__(kPrepThreads)
 replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restrict__ C,
-                        const T* __restrict__ dt) {
+                        const T* __restrict__ dt, int overlap) {
   using TL = Tile<P, N>;
   extern __shared__ float4 smem4[];
   __shared__ int4 s_meta;
@@ -54,6 +54,7 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
       if (g == 0) sv.plan[b] = make_int4(start, n, kPlanBad, epoch);
       set_status(sv.status, REPLAY_DEV_BAD_META);
     }
+    if (overlap) griddep_wait();
     return;
   }
   const bool flush = k >= sv.L;
@@ -64,6 +65,20 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
                        sv.G);
   }
   const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
+  if (!flush) {  // this token's B (the group's) and dt (each head's) into ring slot start + n
+    // An empty ring means the previous step flushed after all (the host expected it not to):
+    // its fold may still be reading this slot, so wait for it to complete first.
+    if (overlap && n == 0) griddep_wait();
+    constexpr int EPC = 16 / sizeof(T), BC = N / EPC;
+    const int slot = ring_slot(start, n, cap);
+    T* bslot = static_cast<T*>(sv.bbuf) + ((static_cast<size_t>(b) * sv.G + g) * cap + slot) * N;
+    for (int c = tid; c < BC; c += kPrepThreads)
+      *reinterpret_cast<uint4*>(bslot + c * EPC) = *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+    for (int hh = tid; hh < sv.hpg; hh += kPrepThreads) {
+      const size_t slab = static_cast<size_t>(b) * sv.H + g * sv.hpg + hh;
+      static_cast<T*>(sv.dtbuf)[slab * cap + slot] = dt[slab];
+    }
+  }
   // One round trip for everything: the k records' B and this token's C go to shared memory by
   // cp.async (non-flush only), and meanwhile every head's k dt values (when they fit).
   T* sb = reinterpret_cast<T*>(smem4);  // [k][N] B, then [N] C
@@ -116,6 +131,7 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
       if (live && s < k) cf[s] = flush ? rw.w : rw.w * s_bc[s];
       if (live && s == 0) cf[cap] = rw.gam;
     }
+    if (overlap) griddep_wait();  // this grid completes after the previous step's kernels
     return;
   }
   for (int hh = warp; hh < sv.hpg; hh += kPrepWarps) {
@@ -133,6 +149,7 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
     if (lane + 32 < k) cf[lane + 32] = flush ? rw.w1 : rw.w1 * s_bc[lane + 32];
     if (lane == 0) cf[cap] = rw.gam;
   }
+  if (overlap) griddep_wait();  // this grid completes after the previous step's kernels
 }
 
 // The state bytes of slabs [slab, slab + nslab) as a per-head kernel reads them: the FP32
@@ -205,6 +222,7 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
   const float Dh = sv.D[h];
 
   griddep_wait();  // plan and coefficients of this step are written
+  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y;
   if (pl.z == kPlanBad) {
@@ -222,18 +240,11 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
     record_terms<RPW, T>(x_of, cf, k, warp, lane, xr);
     const float sum = tile_rows_dot<P, N>(hv, cv, cf[cap], xr, lane);
     if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
-    // append this token's record at ring slot start + n (B once per group, by its first head)
+    // append this token's x at ring slot start + n
     const int slot = ring_slot(start, n, cap);
-    if (tid < XC) {
+    if (tid < XC)  // (the prep kernel appends B and dt)
       *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
           *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
-    } else if (blockIdx.x == 0 && tid < XC + BC) {
-      const int c = tid - XC;
-      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
-          *reinterpret_cast<const uint4*>(B + bo + c * EPC);
-    } else if (tid == XC + BC) {
-      ring.dt[slot] = dt[slab];
-    }
     return;
   }
 
@@ -373,6 +384,7 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
 
   griddep_wait();  // plan and coefficients of this step are written
+  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y, k = n + 1;
   auto x_of_head = [&](int hh, int s) {
@@ -429,16 +441,9 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
       const float sum = warp_transpose_reduce<RPW>(part, lane);
       if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
       const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
-      if (tid < XC) {
+      if (tid < XC)  // (the prep kernel appends B and dt)
         *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
             *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
-      } else if (blockIdx.x == 0 && hh == 0 && tid < XC + BC) {
-        const int c = tid - XC;
-        *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
-            *reinterpret_cast<const uint4*>(B + bo + c * EPC);
-      } else if (tid == XC + BC) {
-        ring.dt[slot] = dt[slab];
-      }
     }
     return;
   }
@@ -496,6 +501,7 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   const float Dh = sv.D[h];
 
   griddep_wait();  // plan and coefficients of this step are written
+  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y, k = n + 1;
   const float* cf = sv.coef + static_cast<size_t>(slab) * (cap + 1);
@@ -528,16 +534,9 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
     const float sum = smem_rows_dot<P, N>(s_h, cv, cf[cap], xr, warp, lane);
     if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
     const int slot = ring_slot(start, n, cap);
-    if (tid < XC) {
+    if (tid < XC)  // (the prep kernel appends B and dt)
       *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
           *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
-    } else if (blockIdx.x == 0 && tid < XC + BC) {
-      const int c = tid - XC;
-      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
-          *reinterpret_cast<const uint4*>(B + bo + c * EPC);
-    } else if (tid == XC + BC) {
-      ring.dt[slot] = dt[slab];
-    }
     return;
   }
 
@@ -648,6 +647,7 @@ replay_step_copy_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
 
   griddep_wait();  // plan and coefficients of this step are written
+  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y;
   if (pl.z == kPlanBad) {
@@ -684,17 +684,10 @@ replay_step_copy_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
       }
       const float sum = warp_transpose_reduce<RPW>(part, lane);
       if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
-      // append this head's record at ring slot start + n (B once per group)
-      if (tid < XC) {
+      // append this head's x at ring slot start + n
+      if (tid < XC)  // (the prep kernel appends B and dt)
         *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
             *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
-      } else if (blockIdx.x == 0 && hh == 0 && tid < XC + BC) {
-        const int c = tid - XC;
-        *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
-            *reinterpret_cast<const uint4*>(B + bo + c * EPC);
-      } else if (tid == XC + BC) {
-        ring.dt[slot] = dt[slab];
-      }
     }
     return;
   }
@@ -866,6 +859,7 @@ replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restric
   const float xk0 = to_f(x[xow + lane]), xk1 = to_f(x[xow + lane + 32]);
 
   griddep_wait();  // plan and coefficients of this step are written
+  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y;
   if (pl.z == kPlanBad) {
@@ -942,17 +936,11 @@ replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restric
     const float Dh = sv.D[hw];
     y[xow + lane] = fmaf(Dh, xk0, fmaf(gsc, s_y[warp][lane], ex0));
     y[xow + lane + 32] = fmaf(Dh, xk1, fmaf(gsc, s_y[warp][lane + 32], ex1));
-    // append this head's record at ring slot start + n (B once per group: warp 0 of the
-    // group's first CTA)
+    // append this head's x at ring slot start + n
     const int slot = ring_slot(start, n, cap);
-    if (lane < XC)
+    if (lane < XC)  // (the prep kernel appends B and dt)
       *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + lane * EPC) =
           *reinterpret_cast<const uint4*>(x + xow + lane * EPC);
-    if (lane == 31) ring.dt[slot] = dt[slabw];
-    if (blockIdx.x == 0 && warp == 0)
-      for (int c = lane; c < BC; c += 32)
-        *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
-            *reinterpret_cast<const uint4*>(B + bo + c * EPC);
     return;
   }
 
@@ -1118,28 +1106,31 @@ replay_step_fused_kernel(StoreView sv, const T* __restrict__ x, const T* __restr
   append_record<P, N, T>(ring, im, cap, ring_slot(start, n, cap), blockIdx.x == 0, dtcur);
 }
 
-// Calls with at most this many (sequence, head) slabs take the fused kernel.
-constexpr long long kFusedMaxSlabs = 1024;
 
 // Launch a per-head kernel as a programmatic dependent of the prep kernel before it.
 template <class... KArgs, class... Args>
-static int pdl_launch(void (*kern)(KArgs...), dim3 grid, size_t smem, cudaStream_t stream, Args... args) {
+static int launch_ex(void (*kern)(KArgs...), dim3 grid, int block, size_t smem, cudaStream_t stream,
+                     bool programmatic, Args... args) {
   if (smem > kSmemNoOptIn &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
     return REPLAY_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = programmatic ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA;
+}
+template <class... KArgs, class... Args>
+static int pdl_launch(void (*kern)(KArgs...), dim3 grid, size_t smem, cudaStream_t stream, Args... args) {
+  return launch_ex(kern, grid, kThreads, smem, stream, true, args...);
 }
 
 // all_n: the ring count every sequence holds before this step when the host knows it (-1
@@ -1148,28 +1139,29 @@ static int pdl_launch(void (*kern)(KArgs...), dim3 grid, size_t smem, cudaStream
 // (more slabs in flight for the FP32 read and write); otherwise a read copy takes the
 // several-heads-per-CTA kernels built for the small copy reads.
 template <int P, int N, class T, int RC>
-static int launch(const StoreView& sv, int all_n, const void* x, const void* B, const void* C, const void* dt,
-                  float* y, cudaStream_t stream) {
+static int launch(const StoreView& base, int all_n, int parity, int overlap, const void* x, const void* B,
+                  const void* C, const void* dt, float* y, cudaStream_t stream) {
   const T *tx = static_cast<const T*>(x), *tB = static_cast<const T*>(B), *tC = static_cast<const T*>(C),
           *tdt = static_cast<const T*>(dt);
-  if (static_cast<long long>(sv.batch) * sv.H <= kFusedMaxSlabs) {
+  if (!step_runs_prep(base)) {
     auto fused = replay_step_fused_kernel<P, N, T, RC>;
-    const size_t fsmem = smem_plan_bytes<P, N>(whole_image_bytes<P, N, T>(sv.cap), sv.cap);
+    const size_t fsmem = smem_plan_bytes<P, N>(whole_image_bytes<P, N, T>(base.cap), base.cap);
     if (fsmem > kSmemNoOptIn &&
         cudaFuncSetAttribute(fused, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(fsmem)) !=
             cudaSuccess)
       return REPLAY_ECUDA;
-    fused<<<dim3(sv.hpg, sv.G, sv.batch), kThreads, fsmem, stream>>>(sv, tx, tB, tC, tdt, y);
+    fused<<<dim3(base.hpg, base.G, base.batch), kThreads, fsmem, stream>>>(base, tx, tB, tC, tdt, y);
     return cudaGetLastError() == cudaSuccess ? REPLAY_OK : REPLAY_ECUDA;
   }
-  auto prep = replay_step_prep_kernel<P, N, T>;
+  StoreView sv = base;  // this step's plan and coefficient buffer (consecutive steps alternate)
+  sv.plan += static_cast<size_t>(parity) * sv.batch;
+  sv.coef += static_cast<size_t>(parity) * sv.batch * sv.H * (sv.cap + 1);
+  // With overlap the prep is a programmatic dependent of the previous step's per-head kernel:
+  // it starts as that kernel's CTAs retire and waits for it only before it completes.
   const size_t psmem = static_cast<size_t>(sv.cap + 1) * N * sizeof(T);
-  if (psmem > kSmemNoOptIn &&
-      cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
-          cudaSuccess)
-    return REPLAY_ECUDA;
-  prep<<<dim3(sv.G, sv.batch), kPrepThreads, psmem, stream>>>(sv, tB, tC, tdt);
-  if (cudaGetLastError() != cudaSuccess) return REPLAY_ECUDA;
+  const int prc = launch_ex(replay_step_prep_kernel<P, N, T>, dim3(sv.G, sv.batch), kPrepThreads, psmem, stream,
+                            overlap != 0, sv, tB, tC, tdt, overlap);
+  if (prc != REPLAY_OK) return prc;
   const size_t smem = fold_staging_bytes<P, N>(sv.cap);
   const bool all_flush = all_n >= 0 && all_n + 1 >= sv.L;
   if constexpr (RC == REPLAY_RC_NVFP4 && N == 128) {
@@ -1204,11 +1196,11 @@ static int launch(const StoreView& sv, int all_n, const void* x, const void* B, 
                     tdt, y, all_flush ? 1 : 0);
 }
 
-int launch_step(const StoreView& sv, const Shape& sh, int all_n, const void* x, const void* B, const void* C,
-                const void* dt, float* y, cudaStream_t stream) {
+int launch_step(const StoreView& sv, const Shape& sh, int all_n, int parity, int overlap, const void* x,
+                const void* B, const void* C, const void* dt, float* y, cudaStream_t stream) {
 #define RSSM_STEP(NN, TT, RCC)                                                  \
   if (sh.N == NN && sh.in_dtype == RSSM_DTYPE_OF(TT) && sh.read_copy == RCC)    \
-    return launch<64, NN, TT, RCC>(sv, all_n, x, B, C, dt, y, stream);
+    return launch<64, NN, TT, RCC>(sv, all_n, parity, overlap, x, B, C, dt, y, stream);
   RSSM_FOR_EACH_CONFIG(RSSM_STEP)
 #undef RSSM_STEP
   return REPLAY_EUNSUPPORTED;

@@ -13,6 +13,11 @@ struct replay_store {
   // full reset, a load or a flush, advanced by each step; -1 (unknown) after a masked reset,
   // a verify or a commit, whose effect depends on device data. Picks kernels only.
   int all_n;
+  // Steps alternate between two plan and coefficient buffers (step_parity: the next step's),
+  // and a step may start its prep kernel while the previous step's per-head kernel runs when
+  // that step is known to have flushed no sequence and ran through the prep (prev_nonflush).
+  int step_parity;
+  int prev_nonflush;
 };
 
 // The step's hint, and the count after a step launched with it.

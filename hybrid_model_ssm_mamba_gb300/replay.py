@@ -300,8 +300,8 @@ class ReplayStore:
             "bscale": (torch.uint8, (Bz, H, P, N // 16) if c.read_copy == REPLAY_RC_NVFP4 else (0,)),
             "xbuf": (dt, (Bz, H, cap, P)), "bbuf": (dt, (Bz, G, cap, N)), "dtbuf": (dt, (Bz, H, cap)),
             "meta": (torch.int32, (Bz, 4)), "arrive": (torch.int32, (Bz,)), "status": (torch.int32, (1,)),
-            "plan": (torch.int32, (Bz, 4)),
-            "coef": (torch.float32, (Bz, H, c.max_draft_T + 1, cap + 1)),
+            "plan": (torch.int32, (2, Bz, 4)),
+            "coef": (torch.float32, (Bz, H, max(c.max_draft_T + 1, 2), cap + 1)),
         }[name]
         tdt, shape = spec
         nbytes = torch.empty((), dtype=tdt).element_size()

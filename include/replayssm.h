@@ -127,9 +127,11 @@ typedef struct replay_config {
  *          number 0, so it is 1 after a load and grows by one at each flush)
  *   arrive per sequence int32 counter (internal; zero between calls)
  *   status int32 device status word (REPLAY_DEV_* bits)
- *   plan   per sequence int32 x4      (internal, per step: the pointer the step runs on)
- *   coef   FP32 [batch][H][T+1][cap+1] (internal, per call: record weights and decays;
- *          T = max_draft_T; a step uses block 0, a verify blocks 0..T)
+ *   plan   2 x per sequence int32 x4  (internal, per step: the pointer the step runs on;
+ *          consecutive steps alternate between the two)
+ *   coef   FP32 [batch][H][max(T+1,2)][cap+1] (internal, per call: record weights and
+ *          decays; T = max_draft_T; a step uses one of the region's first two blocks of
+ *          batch x H x (cap+1) values, alternating, a verify the region as [batch][H][T+1][cap+1])
  * cap = window_L when max_draft_T == 0, else window_L + 2*max_draft_T - 1: the most
  * records a sequence can hold (window_L - 1 + T committed before a verify folds them)
  * plus T drafts written beyond them while those are being folded. */
