@@ -145,6 +145,7 @@ int replay_alloc(const replay_config* c, void* workspace, size_t workspace_bytes
   sv.cap = L.cap;
   sv.tmax = c->max_draft_T;
   sv.shared = c->shared_checkpoint;
+  sv.prep_appends = c->read_copy != REPLAY_RC_NONE;
   int dev = 0;
   sv.sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -200,9 +201,12 @@ int replay_step(replay_store* st, const void* x, const void* B, const void* C, c
     return REPLAY_EBADARG;
   if (!aligned16(x) || !aligned16(B) || !aligned16(C)) return REPLAY_EBADARG;
   const int all_n = st->all_n;
-  const int rc = rssm::launch_step(st->sv, st->sh, all_n, st->step_parity, st->prev_nonflush, x, B, C, dt, y,
+  // (stores without a read copy never overlap steps: one buffer, the per-head kernels append)
+  const int parity = st->sv.prep_appends ? st->step_parity : 0;
+  const int rc = rssm::launch_step(st->sv, st->sh, all_n, parity, st->prev_nonflush, x, B, C, dt, y,
                                    as_stream(stream));
-  st->prev_nonflush = rc == REPLAY_OK && all_n >= 0 && all_n + 1 < st->cfg.window_L && rssm::step_runs_prep(st->sv);
+  st->prev_nonflush = rc == REPLAY_OK && st->sv.prep_appends && all_n >= 0 && all_n + 1 < st->cfg.window_L &&
+                      rssm::step_runs_prep(st->sv);
   if (rc == REPLAY_OK) {
     st->all_n = advance_all_n(st);
     st->step_parity ^= 1;

@@ -49,6 +49,8 @@ struct StoreView {
   int batch, H, G, hpg, L, cap, tmax;
   int shared;     // 1: the read copy is the checkpoint (no FP32 checkpoint)
   int sms;        // SMs of the device the store lives on (0: unknown, no L2 prefetch)
+  int prep_appends;  // 1: a step's prep kernel appends the token's B and dt records (stores
+                     // with a read copy, whose steps overlap); 0: the per-head kernels do
 };
 
 // Bulk prefetch of `bytes` (a multiple of 16, from a 16-byte aligned address) into L2: one

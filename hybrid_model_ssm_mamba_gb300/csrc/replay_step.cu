@@ -65,7 +65,7 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
                        sv.G);
   }
   const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
-  if (!flush) {  // this token's B (the group's) and dt (each head's) into ring slot start + n
+  if (!flush && sv.prep_appends) {  // this token's B (the group's) and dt (each head's) into slot start + n
     // An empty ring means the previous step flushed after all (the host expected it not to):
     // its fold may still be reading this slot, so wait for it to complete first.
     if (overlap && n == 0) griddep_wait();
@@ -222,7 +222,9 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
   const float Dh = sv.D[h];
 
   griddep_wait();  // plan and coefficients of this step are written
-  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
+  // (read-copy stores only: there the next step's prep may overlap this kernel; the trigger
+  // instruction, even when not executed, measurably slows these kernels, so FP32 ones lack it)
+  if constexpr (RC != REPLAY_RC_NONE) griddep_launch_dependents();
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y;
   if (pl.z == kPlanBad) {
@@ -240,11 +242,18 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
     record_terms<RPW, T>(x_of, cf, k, warp, lane, xr);
     const float sum = tile_rows_dot<P, N>(hv, cv, cf[cap], xr, lane);
     if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
-    // append this token's x at ring slot start + n
+    // append this token's record at ring slot start + n (B and dt here unless the prep does)
     const int slot = ring_slot(start, n, cap);
-    if (tid < XC)  // (the prep kernel appends B and dt)
+    if (tid < XC) {
       *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
           *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
+    } else if (!sv.prep_appends && blockIdx.x == 0 && tid < XC + BC) {  // B once per group
+      const int c = tid - XC;
+      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+          *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+    } else if (!sv.prep_appends && tid == XC + BC) {
+      ring.dt[slot] = dt[slab];
+    }
     return;
   }
 
@@ -384,7 +393,7 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
 
   griddep_wait();  // plan and coefficients of this step are written
-  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
+  griddep_launch_dependents();  // after the wait: the next step's prep may start
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y, k = n + 1;
   auto x_of_head = [&](int hh, int s) {
@@ -441,9 +450,16 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
       const float sum = warp_transpose_reduce<RPW>(part, lane);
       if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
       const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
-      if (tid < XC)  // (the prep kernel appends B and dt)
+      if (tid < XC) {
         *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
             *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
+      } else if (!sv.prep_appends && blockIdx.x == 0 && hh == 0 && tid < XC + BC) {
+        const int c = tid - XC;
+        *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+            *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+      } else if (!sv.prep_appends && tid == XC + BC) {
+        ring.dt[slot] = dt[slab];
+      }
     }
     return;
   }
@@ -501,7 +517,6 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   const float Dh = sv.D[h];
 
   griddep_wait();  // plan and coefficients of this step are written
-  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y, k = n + 1;
   const float* cf = sv.coef + static_cast<size_t>(slab) * (cap + 1);
@@ -534,9 +549,16 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
     const float sum = smem_rows_dot<P, N>(s_h, cv, cf[cap], xr, warp, lane);
     if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
     const int slot = ring_slot(start, n, cap);
-    if (tid < XC)  // (the prep kernel appends B and dt)
+    if (tid < XC) {
       *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
           *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
+    } else if (!sv.prep_appends && blockIdx.x == 0 && tid < XC + BC) {  // B once per group
+      const int c = tid - XC;
+      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+          *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+    } else if (!sv.prep_appends && tid == XC + BC) {
+      ring.dt[slot] = dt[slab];
+    }
     return;
   }
 
@@ -647,7 +669,7 @@ replay_step_copy_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   const int myrow = warp * RPW + transpose_index<RPW>(lane);
 
   griddep_wait();  // plan and coefficients of this step are written
-  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
+  griddep_launch_dependents();  // after the wait: the next step's prep may start
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y;
   if (pl.z == kPlanBad) {
@@ -684,10 +706,17 @@ replay_step_copy_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
       }
       const float sum = warp_transpose_reduce<RPW>(part, lane);
       if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
-      // append this head's x at ring slot start + n
-      if (tid < XC)  // (the prep kernel appends B and dt)
+      // append this head's record at ring slot start + n (B and dt here unless the prep does)
+      if (tid < XC) {
         *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
             *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
+      } else if (!sv.prep_appends && blockIdx.x == 0 && hh == 0 && tid < XC + BC) {
+        const int c = tid - XC;
+        *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+            *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+      } else if (!sv.prep_appends && tid == XC + BC) {
+        ring.dt[slot] = dt[slab];
+      }
     }
     return;
   }
@@ -859,7 +888,7 @@ replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restric
   const float xk0 = to_f(x[xow + lane]), xk1 = to_f(x[xow + lane + 32]);
 
   griddep_wait();  // plan and coefficients of this step are written
-  griddep_launch_dependents();  // after the wait: the next step's prep needs this one's complete
+  griddep_launch_dependents();  // after the wait: the next step's prep may start
   const int4 pl = sv.plan[b];
   const int start = pl.x, n = pl.y;
   if (pl.z == kPlanBad) {
@@ -936,11 +965,18 @@ replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restric
     const float Dh = sv.D[hw];
     y[xow + lane] = fmaf(Dh, xk0, fmaf(gsc, s_y[warp][lane], ex0));
     y[xow + lane + 32] = fmaf(Dh, xk1, fmaf(gsc, s_y[warp][lane + 32], ex1));
-    // append this head's x at ring slot start + n
+    // append this head's record at ring slot start + n (B and dt here unless the prep does)
     const int slot = ring_slot(start, n, cap);
-    if (lane < XC)  // (the prep kernel appends B and dt)
+    if (lane < XC)
       *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + lane * EPC) =
           *reinterpret_cast<const uint4*>(x + xow + lane * EPC);
+    if (!sv.prep_appends) {
+      if (lane == 31) ring.dt[slot] = dt[slabw];
+      if (blockIdx.x == 0 && warp == 0)
+        for (int c = lane; c < BC; c += 32)
+          *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+              *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+    }
     return;
   }
 
