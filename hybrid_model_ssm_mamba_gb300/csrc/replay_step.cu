@@ -21,6 +21,13 @@
 //     Gamma_k h0 . C and sum_s c_s x_s. A flush stages u_s = w_s x_s and B_s in FP32 shared
 //     memory, applies the rank-k update, reads y from the new state and writes the
 //     checkpoint (and read copy) once.
+// Which per-head kernel runs is chosen on the host and never changes results (each handles
+// any plan): replay_step_read_kernel (FP32 checkpoint, phase known: the slab by one bulk copy
+// into shared memory), replay_step_copy_read_kernel / replay_step_copy_kernel (bf16, E4M3,
+// FP16 read copies, several heads per CTA), replay_step_fp4_kernel (NVFP4 read copy, h0 . C
+// on the tensor cores), replay_step_kernel (the rest: unknown phase, flushes of read-copy
+// stores); calls of at most 1024 slabs take replay_step_fused_kernel and no prep. With a
+// read copy, a step's prep may run during the previous step's per-head kernel (see launch).
 #include "launch.h"
 #include "replay_core.cuh"
 
