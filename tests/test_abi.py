@@ -28,6 +28,20 @@ def test_layout_of_nemotron_layer():
     assert R.replay_store_bytes(cfg) == L.total
 
 
+@pytest.mark.parametrize("T", [0, 1, 4])
+def test_layout_step_buffers(T):
+    """Consecutive steps alternate between two plans and two coefficient blocks (a step's prep
+    may write its own while the previous step's per-head kernel reads the other): the plan
+    region holds 2 x batch int4, the coefficient region at least two batch x H x (cap + 1)
+    blocks, and a verify's [batch][H][T + 1][cap + 1] when T + 1 > 2."""
+    cfg = R.ReplayConfig(64, 16, 64, 128, 2, 8, T, R.REPLAY_BF16, R.REPLAY_RC_BF16)
+    L = R.replay_layout_of(cfg)
+    block = 64 * 16 * (L.cap + 1) * 4
+    assert L.coef - L.plan >= 2 * 64 * 16
+    assert L.total - L.coef >= max(T + 1, 2) * block
+    assert L.total - L.coef < max(T + 1, 2) * block + 256
+
+
 def test_layout_ring_capacity_and_read_copies():
     cfg = R.ReplayConfig(512, 8, 64, 128, 1, 16, 4, R.REPLAY_F32, R.REPLAY_RC_FP8E4M3)
     L = R.replay_layout_of(cfg)
