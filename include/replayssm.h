@@ -46,7 +46,9 @@
 extern "C" {
 #endif
 
-#define REPLAY_ABI_VERSION 2
+/* 3: the workspace holds two step plans and at least two coefficient blocks (replay_layout
+ * sizes changed); status bit REPLAY_DEV_COPY_TIMEOUT. */
+#define REPLAY_ABI_VERSION 3
 
 /* element types of x, B, C, dt and of the ring records */
 #define REPLAY_F32 0

@@ -12,7 +12,7 @@ def test_exports_every_header_symbol(lib):
     assert len(names) >= 17
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.replay_abi_version() == 2
+    assert lib.replay_abi_version() == 3
     assert lib.replay_strerror(-3) == b"capacity exceeded"
 
 
