@@ -22,7 +22,11 @@
  *    caller and is passed as plain device pointers. The library owns only the small
  *    host handle returned by replay_alloc. It allocates no device memory.
  *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream). Every
- *    device call is asynchronous on that stream and launches on no other stream.
+ *    device call is asynchronous on that stream and launches on no other stream. The calls
+ *    on one store must run in the order they are made: issue them on one stream, or order
+ *    the streams with events. Two consecutive replay_step calls on one stream may overlap on
+ *    the GPU (a store with a read copy starts a step's first kernel while the previous
+ *    step's last one finishes; the results are those of running them one after the other).
  *  - Return codes: REPLAY_OK, or a negative REPLAY_E* code for errors found on the host
  *    (nothing is launched then). Errors found on the device never trap: they set bits of
  *    the store's status word (REPLAY_DEV_*), read with replay_status.
