@@ -235,7 +235,9 @@ int replay_status(replay_store* st, int* status_out, int clear, void* stream);
  *    (16 KiB of counters, 64 KiB of plans, 4 MiB of coefficients) exists on every GPU that
  *    loads the library, until the process exits.
  *  - The first call on a device looks up the array's device address (once per device, with
- *    that device current); make that first call before any stream capture.
+ *    that device current); make that first call before any stream capture. The address is
+ *    kept for the life of the process: after cudaDeviceReset (or any teardown of the device's
+ *    primary context) this call must not be used again in that process.
  *  - Each call zeroes the counters it uses (an asynchronous memset on `stream`, no
  *    allocation) before its launch. All calls share the one array, so calls on the same
  *    device that can overlap on the GPU (different streams, no ordering between them) race

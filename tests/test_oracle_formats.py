@@ -234,3 +234,64 @@ def test_nvfp4_error_bound_on_random_slabs():
         bmax = np.abs(h).reshape(16, 8, 16).max(axis=2)
         bback = np.abs(back).reshape(16, 8, 16).max(axis=2)
         assert np.all(np.abs(bback - bmax) <= bmax / 8 + 1e-30), trial
+
+
+# ------------------------------------------------------------------ state rounding of the shared checkpoints
+def test_fp16_sr_state_draw_index_hand_worked():
+    """The draw of element e of slab s written by flush `epoch` is output
+    (epoch * num_slabs + s) * P*N + e of the generator, with s numbered over the whole batch
+    (s = b * H + h for the sequence's place b in the batch, not its place in the subset
+    followed). Here the oracle follows sequences 4 and 1 of a 5-sequence batch (H = 3,
+    P = 2, N = 4, so num_slabs = 15 and P*N = 8) at epoch 2. Six elements sit a hair above
+    or below their own draw between the FP16 neighbours 1 and 1 + 2**-10 (times a power of
+    two), so each rounds the way that draw alone decides; the rest are FP16 values, which
+    stochastic rounding keeps whatever the draw."""
+    H, P, N, epoch, num_slabs = 3, 2, 4, 2, 15
+    # (place in the state, head, row, column) -> draw index, worked by hand:
+    #   slab = seq * 3 + head, elem = row * 4 + column, idx = (2 * 15 + slab) * 8 + elem
+    hand = {
+        (0, 2, 1, 3): 359,   # seq 4: slab 14, elem 7 -> (30 + 14) * 8 + 7
+        (1, 0, 0, 0): 264,   # seq 1: slab 3,  elem 0 -> (30 + 3) * 8 + 0
+        (0, 0, 0, 1): 337,   # seq 4: slab 12, elem 1 -> (30 + 12) * 8 + 1
+        (1, 2, 1, 2): 286,   # seq 1: slab 5,  elem 6 -> (30 + 5) * 8 + 6
+        (0, 1, 0, 2): 346,   # seq 4: slab 13, elem 2 -> (30 + 13) * 8 + 2
+        (1, 1, 1, 0): 276,   # seq 1: slab 4,  elem 4 -> (30 + 4) * 8 + 4
+    }
+    rng = np.random.default_rng(11)
+    grid = F.fp16_decode(rng.integers(0x2000, 0x5000, size=(2, H, P, N)).astype(np.uint16))
+    grid = np.where(rng.random(grid.shape) < 0.5, -grid, grid)
+    h = grid.copy()
+    want = grid.copy()
+    for j, (pos, idx) in enumerate(sorted(hand.items())):
+        u = F.sr_uniform(np.array([idx], dtype=np.uint64))[0]
+        k = int(u * 2 ** 13)                       # the draw's first 13 bits: k / 2**13 <= u
+        up = j % 2 == 0
+        frac = (k + 1) / 2 ** 13 if up else k / 2 ** 13   # above the draw: rounds away from zero
+        scale = 2.0 ** (j - 3) * (-1 if j == 3 else 1)
+        h[pos] = scale * (1.0 + frac * 2.0 ** -10)         # exact in FP32 (13 fraction bits)
+        want[pos] = scale * ((1.0 + 2.0 ** -10) if up else 1.0)
+    got = F.fp16_sr_round_state(h, epoch, [4, 1], num_slabs)
+    assert np.array_equal(got, want)
+
+
+def test_nvfp4_state_rounding_is_per_slab():
+    """A state of several slabs, each built (as in the exactly-representable test) from
+    E2M1 values times E4M3-exact block scales under its own power-of-two slab scale, comes
+    back exactly: each slab takes its own absmax scale and its blocks run along a row. One
+    slab is zero and stays zero."""
+    rng = np.random.default_rng(4)
+    P, N = 16, 64
+    bs_vals = F.e4m3_decode(np.arange(0x38, 0x7F, dtype=np.uint8))   # 1 .. 448
+    h = np.zeros((2, 3, P, N))
+    for b in range(2):
+        for k in range(3):
+            if (b, k) == (1, 2):
+                continue                                          # the zero slab
+            s_g = 2.0 ** -(6 + 3 * (3 * b + k))                   # a different scale per slab
+            s_b = rng.choice(bs_vals, size=(P, N // 16))
+            s_b[rng.integers(P), rng.integers(2)] = 448.0           # in the first 32 columns
+            q = rng.integers(0, 16, size=(P, N)).astype(np.uint8)
+            q[:, ::16] = np.where(rng.random((P, N // 16)) < 0.5, 7, 15)   # each block reaches +-6
+            h[b, k] = (F.e2m1_decode(q).reshape(P, N // 16, 16) * (s_b * s_g)[:, :, None]).reshape(P, N)
+    assert np.array_equal(F.nvfp4_round_state(h), h)
+    assert np.array_equal(F.nvfp4_round_state(h[:, :, :, :32]), h[:, :, :, :32])   # a narrower slab

@@ -133,11 +133,52 @@ def _sr_round_to_nearest(v, u):
     return fm.fp16_encode(v)
 
 
+def _sr_state(index_of):
+    """fp16_sr_round_state with the draw index computed by index_of(epoch, slab, num_slabs, elem)."""
+    def rounded(h, epoch, slabs, num_slabs):
+        h32 = np.asarray(h, dtype=np.float64).astype(np.float32)
+        bsz, H, P, N = h32.shape
+        slab = (np.asarray(slabs, dtype=np.uint64).reshape(-1, 1) * np.uint64(H) +
+                np.arange(H, dtype=np.uint64).reshape(1, -1)).reshape(bsz, H, 1, 1)
+        elem = np.arange(P * N, dtype=np.uint64).reshape(1, 1, P, N)
+        idx = index_of(np.uint64(epoch), slab, np.uint64(num_slabs), np.uint64(P * N), elem, bsz, H)
+        return fm.fp16_decode(fm.fp16_sr_encode(h32, fm.sr_uniform(idx)))
+    return rounded
+
+
+def _sr_local_slab(e, s, n, pn, elem, bsz, H):      # slabs numbered within the followed subset
+    local = (np.arange(bsz, dtype=np.uint64).reshape(-1, 1) * np.uint64(H) +
+             np.arange(H, dtype=np.uint64).reshape(1, -1)).reshape(bsz, H, 1, 1)
+    return (e * n + local) * pn + elem
+
+
+def _nvfp4_state_blocks_down_columns(h):
+    h32 = np.asarray(h, dtype=np.float64).astype(np.float32)
+    out = np.empty(h32.shape, dtype=np.float64)
+    for idx in np.ndindex(*h32.shape[:-2]):
+        out[idx] = fm.nvfp4_slab_dequantize(*fm.nvfp4_slab_quantize(h32[idx].T)).T
+    return out
+
+
+def _nvfp4_state_one_scale(h):
+    h32 = np.asarray(h, dtype=np.float64).astype(np.float32)
+    P, N = h32.shape[-2:]
+    flat = h32.reshape(-1, N)
+    return fm.nvfp4_slab_dequantize(*fm.nvfp4_slab_quantize(flat)).reshape(h32.shape)
+
+
 FORMAT_MUTATIONS = {
     "e2m1_ties_away_from_zero": ("e2m1_encode", _e2m1_ties_away),
     "nvfp4_nibbles_swapped": ("nvfp4_pack", _pack_swapped),
     "nvfp4_slab_scale_missing_6": ("nvfp4_slab_quantize", _slab_scale_without_e2m1_max),
     "fp16_sr_is_round_to_nearest": ("fp16_sr_encode", _sr_round_to_nearest),
+    "sr_index_epoch_and_slab_swapped": (
+        "fp16_sr_round_state", _sr_state(lambda e, s, n, pn, elem, bsz, H: (s * n + e) * pn + elem)),
+    "sr_index_epoch_off_by_one": (
+        "fp16_sr_round_state", _sr_state(lambda e, s, n, pn, elem, bsz, H: ((e + np.uint64(1)) * n + s) * pn + elem)),
+    "sr_index_subset_numbering_ignored": ("fp16_sr_round_state", _sr_state(_sr_local_slab)),
+    "nvfp4_state_blocks_down_columns": ("nvfp4_round_state", _nvfp4_state_blocks_down_columns),
+    "nvfp4_state_one_scale_for_all_slabs": ("nvfp4_round_state", _nvfp4_state_one_scale),
 }
 
 
