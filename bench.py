@@ -212,14 +212,17 @@ def run_replay(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    w = WORKLOAD
+    w = dict(WORKLOAD)
+    if args.kernels_only and args.batch:      # diagnostics: a smaller batch for profiler runs
+        w["batch"] = args.batch
     L = w["L"]
     shape = sg.LayerShape(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["dtype"])
     A, D = sg.head_params(w["nheads"], 0)
     rc_code = {"none": R.REPLAY_RC_NONE, "bf16": R.REPLAY_RC_BF16, "e4m3": R.REPLAY_RC_FP8E4M3,
                "fp16": R.REPLAY_RC_FP16, "nvfp4": R.REPLAY_RC_NVFP4}[args.read_copy]
     cfg = R.ReplayConfig(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], L, 0,
-                         R.REPLAY_BF16, rc_code, int(args.shared_checkpoint))
+                         R.REPLAY_BF16, rc_code, int(args.shared_checkpoint),
+                         R.REPLAY_CKPT_F16_SR if args.fp16_checkpoint else R.REPLAY_CKPT_F32)
     st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
     dev, host = window_inputs(shape, rank, L, torch)
     y = torch.empty(w["batch"], w["nheads"], w["headdim"], device="cuda")
@@ -472,22 +475,23 @@ def run_speculative(torch, R, calls=64, distinct=16):
 
 
 def run_read_copies(torch, R, dev, steps=10):
-    """The headline window with a bf16, E4M3 or FP16 read copy of the FP32 checkpoint, and
-    with a shared bf16, E4M3 or FP16 (stochastically rounded) checkpoint."""
+    """The headline window with a bf16, E4M3, FP16 or NVFP4 read copy of the FP32 checkpoint,
+    with a shared bf16, E4M3, FP16 (stochastically rounded) or NVFP4 checkpoint, and with an
+    FP16 stochastically rounded checkpoint beside an NVFP4 read copy."""
     w = WORKLOAD
     L = w["L"]
     A, D = sg.head_params(w["nheads"], 0)
     y = torch.empty(w["batch"], w["nheads"], w["headdim"], device="cuda")
     out = {}
-    for name, rc, fmt, shared in (("bf16", R.REPLAY_RC_BF16, "bf16", 0), ("e4m3", R.REPLAY_RC_FP8E4M3, "e4m3", 0),
-                                  ("fp16", R.REPLAY_RC_FP16, "fp16", 0), ("nvfp4", R.REPLAY_RC_NVFP4, "nvfp4", 0),
-                                  ("shared_bf16", R.REPLAY_RC_BF16, "bf16", 1),
-                                  ("shared_e4m3", R.REPLAY_RC_FP8E4M3, "e4m3", 1),
-                                  ("shared_fp16_sr", R.REPLAY_RC_FP16, "fp16", 1),
-                                  ("shared_nvfp4", R.REPLAY_RC_NVFP4, "nvfp4", 1)):
+    for name, rc, fmt, shared, ckpt in (
+            ("bf16", R.REPLAY_RC_BF16, "bf16", 0, 0), ("e4m3", R.REPLAY_RC_FP8E4M3, "e4m3", 0, 0),
+            ("fp16", R.REPLAY_RC_FP16, "fp16", 0, 0), ("nvfp4", R.REPLAY_RC_NVFP4, "nvfp4", 0, 0),
+            ("shared_bf16", R.REPLAY_RC_BF16, "bf16", 1, 0), ("shared_e4m3", R.REPLAY_RC_FP8E4M3, "e4m3", 1, 0),
+            ("shared_fp16_sr", R.REPLAY_RC_FP16, "fp16", 1, 0), ("shared_nvfp4", R.REPLAY_RC_NVFP4, "nvfp4", 1, 0),
+            ("fp16_sr_ckpt_nvfp4", R.REPLAY_RC_NVFP4, "nvfp4", 0, R.REPLAY_CKPT_F16_SR)):
         rcb, slab_scale = RC_BYTES[fmt]
         cfg = R.ReplayConfig(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], L, 0,
-                             R.REPLAY_BF16, rc, shared)
+                             R.REPLAY_BF16, rc, shared, ckpt)
         st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
         for _ in range(2):
             for t in range(L):
@@ -512,7 +516,8 @@ def run_read_copies(torch, R, dev, steps=10):
         torch.cuda.synchronize()
         us = np.array([a.elapsed_time(b) for a, b in ev]).reshape(steps, L) * 1e3
         nf_bytes = sum(step_bytes(w, t, False, rc_bytes=rcb, slab_scale=slab_scale) for t in range(L - 1))
-        fl_bytes = step_bytes(w, L - 1, True, rc_bytes=rcb, shared=bool(shared), slab_scale=slab_scale)
+        fl_bytes = step_bytes(w, L - 1, True, rc_bytes=rcb, shared=bool(shared), slab_scale=slab_scale,
+                              state_bytes=2 if ckpt else 4)
         out[name] = {"tokens_per_s": w["batch"] * L / (window_us * 1e-6),
                      "window_us": window_us,
                      "nonflush_launch_us": float(us[:, :-1].mean()),
@@ -714,6 +719,10 @@ def main(argv=None):
                     help="diagnostics: give the timed store this read copy (the benchmark line is 'none')")
     ap.add_argument("--shared-checkpoint", action="store_true",
                     help="diagnostics: the read copy is the checkpoint (needs --read-copy)")
+    ap.add_argument("--fp16-checkpoint", action="store_true",
+                    help="diagnostics: keep the checkpoint in FP16 with stochastic rounding (needs --read-copy)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="diagnostics with --kernels-only: sequences per GPU (default: the workload's 256)")
     ap.add_argument("--kernels-only", action="store_true",
                     help="diagnostics: time only the replay windows and print a short line (for ncu runs)")
     ap.add_argument("--verify-only", action="store_true",

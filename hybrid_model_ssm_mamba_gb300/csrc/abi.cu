@@ -63,6 +63,12 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   if (c->read_copy == REPLAY_RC_NVFP4 && c->dstate != 128) return REPLAY_EUNSUPPORTED;
   if (c->shared_checkpoint != 0 && (c->shared_checkpoint != 1 || c->read_copy == REPLAY_RC_NONE))
     return REPLAY_EBADARG;
+  if (c->checkpoint_format != REPLAY_CKPT_F32 && c->checkpoint_format != REPLAY_CKPT_F16_SR) return REPLAY_EBADARG;
+  if (c->checkpoint_format == REPLAY_CKPT_F16_SR) {
+    if (c->shared_checkpoint != 0 || c->read_copy == REPLAY_RC_NONE || c->read_copy == REPLAY_RC_FP16)
+      return REPLAY_EBADARG;
+    if (c->dstate > 128) return REPLAY_EUNSUPPORTED;
+  }
   if (c->max_draft_T > 8) return REPLAY_ECAPACITY;
   const long long cap = c->max_draft_T > 0 ? static_cast<long long>(c->window_L) + 2LL * c->max_draft_T - 1
                                            : c->window_L;
@@ -82,7 +88,8 @@ int replay_layout_of(const replay_config* c, replay_layout* out) {
   };
   replay_layout L;
   L.cap = static_cast<int>(cap);
-  L.h0 = take(c->shared_checkpoint ? 0 : Bn * H * P * N * 4);  // no FP32 checkpoint when shared
+  const size_t ckpt_bytes = c->shared_checkpoint ? 0 : (c->checkpoint_format == REPLAY_CKPT_F16_SR ? 2 : 4);
+  L.h0 = take(Bn * H * P * N * ckpt_bytes);  // no separate checkpoint when shared
   L.rc = take(Bn * H * P * N / 2 * rc2);
   L.scale = take(slab_scale ? Bn * H * 4 : 0);
   L.bscale = take(c->read_copy == REPLAY_RC_NVFP4 ? Bn * H * P * N / 16 : 0);
@@ -145,6 +152,7 @@ int replay_alloc(const replay_config* c, void* workspace, size_t workspace_bytes
   sv.cap = L.cap;
   sv.tmax = c->max_draft_T;
   sv.shared = c->shared_checkpoint;
+  sv.ckpt16 = c->checkpoint_format == REPLAY_CKPT_F16_SR;
   sv.prep_appends = c->read_copy != REPLAY_RC_NONE;
   int dev = 0;
   sv.sms = 0;
@@ -205,8 +213,9 @@ int replay_step(replay_store* st, const void* x, const void* B, const void* C, c
   const int parity = st->sv.prep_appends ? st->step_parity : 0;
   const int rc = rssm::launch_step(st->sv, st->sh, all_n, parity, st->prev_nonflush, x, B, C, dt, y,
                                    as_stream(stream));
+  // (a step run by the streaming kernel has no prep for the next step's prep to follow)
   st->prev_nonflush = rc == REPLAY_OK && st->sv.prep_appends && all_n >= 0 && all_n + 1 < st->cfg.window_L &&
-                      rssm::step_runs_prep(st->sv);
+                      rssm::step_runs_prep(st->sv) && !rssm::step_streams(st->sv, st->sh, all_n, dt);
   if (rc == REPLAY_OK) {
     st->all_n = advance_all_n(st);
     st->step_parity ^= 1;

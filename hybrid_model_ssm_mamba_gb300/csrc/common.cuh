@@ -48,6 +48,7 @@ struct StoreView {
   const float* D;
   int batch, H, G, hpg, L, cap, tmax;
   int shared;     // 1: the read copy is the checkpoint (no FP32 checkpoint)
+  int ckpt16;     // 1: h0 holds FP16 values written by stochastic rounding (not FP32)
   int sms;        // SMs of the device the store lives on (0: unknown, no L2 prefetch)
   int prep_appends;  // 1: a step's prep kernel appends the token's B and dt records (stores
                      // with a read copy, whose steps overlap); 0: the per-head kernels do
@@ -164,7 +165,9 @@ __device__ __forceinline__ void ld_e4m3_stream(const uint8_t* p, float scale, fl
     o[0] = a.x * scale; o[1] = a.y * scale;
   }
 }
-// Codes are decided in FP32 with an IEEE division by the scale, as the format defines.
+// Codes are decided in FP32 with an IEEE division by the scale, as the format defines. (A
+// multiply by the reciprocal with an exact fallback near the code boundaries was measured: the
+// boundary tests cost as many instructions as the division and added branch stalls.)
 template <int VEC>
 __device__ __forceinline__ void st_e4m3_stream(uint8_t* p, float scale, const float (&v)[VEC]) {
   if constexpr (VEC == 4) {
@@ -383,9 +386,9 @@ __device__ __forceinline__ void st_f16_stream(__half* p, const float (&v)[VEC]) 
   }
 }
 
-// The draws of stochastic rounding: output idx of the splitmix64 sequence (Steele, Lea and
-// Flood, "Fast splittable pseudorandom number generators", OOPSLA 2014) started at kSrSeed;
-// its top 24 bits give u in [0, 1).
+// The draws of stochastic rounding, 16 bits each: draw idx is 16-bit chunk idx mod 4 (most
+// significant first) of output idx / 4 of the splitmix64 sequence (Steele, Lea and Flood, "Fast
+// splittable pseudorandom number generators", OOPSLA 2014) started at kSrSeed; u = chunk / 2^16.
 constexpr unsigned long long kSrSeed = 0x2545F4914F6CDD1Dull;
 __device__ __forceinline__ unsigned long long splitmix64_at(unsigned long long seed, unsigned long long idx) {
   unsigned long long z = seed + (idx + 1ull) * 0x9E3779B97F4A7C15ull;
@@ -497,24 +500,42 @@ __device__ __forceinline__ void store_tile_nvfp4(void* rc, uint8_t* bscale, size
   }
 }
 
+// The same decision with a 16-bit draw u16 (u = u16 / 2^16), in integers for FP16 normals:
+// truncating an FP32 at or above 2^-14 to FP16 drops its 13 low fraction bits t, the fraction of
+// the spacing is t / 2^13 exactly, and u < t / 2^13 iff u16 < 8 t. Magnitudes from 65504 up
+// saturate; FP16 subnormals and zero take the general routine.
+__device__ __forceinline__ unsigned short f16_sr16(float v, unsigned u16) {
+  const unsigned b = __float_as_uint(v), a = b & 0x7fffffffu;
+  const unsigned sign = (b >> 16) & 0x8000u;
+  if (a >= 0x38800000u) {
+    const unsigned mag = (a >> 13) - 0x1C000u;  // FP16 exponent and fraction, truncated
+    if (mag >= 0x7BFFu) return static_cast<unsigned short>(sign | 0x7BFFu);
+    return static_cast<unsigned short>(sign | (mag + (u16 < ((a & 0x1fffu) << 3) ? 1u : 0u)));
+  }
+  return f16_sr(v, static_cast<float>(u16) * 0x1p-16f);
+}
+
 // An FP16 tile by stochastic rounding: element e of slab `slab` (of num_slabs) written by
-// flush `epoch` draws u from index (epoch * num_slabs + slab) * P*N + e.
+// flush `epoch` takes draw (epoch * num_slabs + slab) * P*N + e. A lane's VEC columns start at
+// a multiple of VEC, so they share one generator output (two lanes share it when VEC is 2).
 template <int P, int N>
 __device__ __forceinline__ void store_tile_f16_sr(void* rc, size_t slab, unsigned long long epoch,
                                                   unsigned long long num_slabs, int warp, int lane,
                                                   const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
   using TL = Tile<P, N>;
+  static_assert(TL::VEC == 2 || TL::VEC == 4, "a lane's columns lie within one generator output");
   const unsigned long long base = (epoch * num_slabs + slab) * static_cast<unsigned long long>(P * N);
 #pragma unroll
   for (int i = 0; i < TL::RPW; ++i)
 #pragma unroll
     for (int v = 0; v < TL::NVEC; ++v) {
       const int e0 = TL::row(warp, i) * N + TL::col(lane, v);
+      const unsigned long long z = splitmix64_at(kSrSeed, (base + e0) >> 2);
       unsigned short c[TL::VEC];
 #pragma unroll
       for (int e = 0; e < TL::VEC; ++e) {
-        const float u = static_cast<float>(splitmix64_at(kSrSeed, base + e0 + e) >> 40) * 0x1p-24f;
-        c[e] = f16_sr(hv[i][v * TL::VEC + e], u);
+        const int chunk = (e0 + e) & 3;  // base is a multiple of 4
+        c[e] = f16_sr16(hv[i][v * TL::VEC + e], static_cast<unsigned>(z >> (48 - 16 * chunk)) & 0xffffu);
       }
       __half* p = static_cast<__half*>(rc) + slab * P * N + e0;
       if constexpr (TL::VEC == 4) {

@@ -109,20 +109,51 @@ __device__ __forceinline__ void append_record(const SlabRing<T>& ring, const Rin
   }
 }
 
-// Write a new checkpoint tile: FP32 always, and the read copy cast independently from the
-// same FP32 values ("Benefit 3: Limit error accumulation with separate precisions"). The
-// E4M3 copy takes one FP32 scale per slab, absmax / 448 (1 for an all-zero slab). An FP16
-// copy rounds to nearest even, except when it is itself the checkpoint: then it is rounded
-// stochastically, with draws indexed by the sequence's flush count `epoch` (the FP16
-// recurrence checkpoint with stochastic rounding the post's section "State quantization"
-// cites). Contains CTA barriers when the copy is E4M3.
-template <int P, int N, int RC>
+// Load the checkpoint tile of a slab: FP32, or FP16 widened when the checkpoint is kept in
+// FP16 (the caller handles a shared checkpoint, which is the read copy itself).
+template <int P, int N>
+__device__ __forceinline__ void load_checkpoint(const StoreView& sv, size_t slab, int warp, int lane,
+                                                float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
+  if constexpr (N <= 128) {
+    if (sv.ckpt16) {
+      load_tile_rc<P, N, REPLAY_RC_FP16>(sv.h0, slab, 1.f, warp, lane, hv);
+      return;
+    }
+  }
+  load_tile_f32<P, N>(sv.h0 + slab * P * N, warp, lane, hv);
+}
+
+// Write a new checkpoint tile: FP32 (or FP16 by stochastic rounding, when the checkpoint is
+// kept in FP16), and the read copy cast independently from the same FP32 values ("Benefit 3:
+// Limit error accumulation with separate precisions"). The E4M3 copy takes one FP32 scale per
+// slab, absmax / 448 (1 for an all-zero slab). An FP16 copy rounds to nearest even, except when
+// it is itself the checkpoint: then it is rounded stochastically, with draws indexed by the
+// sequence's flush count `epoch` (the FP16 recurrence checkpoint with stochastic rounding the
+// post's section "State quantization" cites); an FP16 checkpoint beside a read copy takes the
+// same draws. Contains CTA barriers when the copy is E4M3 or NVFP4.
+// The barrier of a whole CTA; kernels whose warps split into groups pass their own.
+struct CtaSync {
+  __device__ void operator()() const { __syncthreads(); }
+};
+
+// (tid: the thread's index among the kThreads threads that write the tile)
+template <int P, int N, int RC, class Sync = CtaSync>
 __device__ __forceinline__ void write_checkpoint(const StoreView& sv, size_t slab, float* s_red,
                                                  const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E],
-                                                 int epoch) {
+                                                 int epoch, Sync sync = Sync()) {
   using TL = Tile<P, N>;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (!sv.shared) store_tile_f32<P, N>(sv.h0 + slab * P * N, warp, lane, hv);  // shared: copy only
+  const int tid = threadIdx.x & (kThreads - 1), warp = tid >> 5, lane = tid & 31;
+  if (!sv.shared) {  // shared: the copy only
+    bool done = false;
+    if constexpr (N <= 128 && RC != REPLAY_RC_NONE && RC != REPLAY_RC_FP16) {
+      if (sv.ckpt16) {  // the FP16 checkpoint, rounded stochastically (draws of write `epoch`)
+        store_tile_f16_sr<P, N>(sv.h0, slab, static_cast<unsigned int>(epoch),
+                                static_cast<unsigned long long>(sv.batch) * sv.H, warp, lane, hv);
+        done = true;
+      }
+    }
+    if (!done) store_tile_f32<P, N>(sv.h0 + slab * P * N, warp, lane, hv);
+  }
   if constexpr (RC == REPLAY_RC_BF16) {
     store_tile_rc<P, N, RC>(sv.rc, slab, 1.f, warp, lane, hv);
   } else if constexpr (RC == REPLAY_RC_FP16) {
@@ -138,9 +169,9 @@ __device__ __forceinline__ void write_checkpoint(const StoreView& sv, size_t sla
 #pragma unroll
       for (int e = 0; e < TL::E; ++e) m = fmaxf(m, fabsf(hv[i][e]));
     m = warp_max(m);
-    __syncthreads();  // s_red may hold an earlier phase's values
+    sync();  // s_red may hold an earlier phase's values
     if (lane == 0) s_red[warp] = m;
-    __syncthreads();
+    sync();
     float amax = s_red[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, s_red[w]);

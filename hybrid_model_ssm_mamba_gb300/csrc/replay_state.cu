@@ -32,7 +32,7 @@ replay_fold_kernel(StoreView sv, float* __restrict__ out) {
     const float scale = RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4 ? sv.scale[slab] : 1.f;
     load_tile_rc<P, N, RC == REPLAY_RC_NONE ? REPLAY_RC_BF16 : RC>(sv.rc, slab, scale, warp, lane, hv, sv.bscale);
   } else {
-    load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    load_checkpoint<P, N>(sv, slab, warp, lane, hv);
   }
   __syncthreads();
   const int start = s_meta.x, n = s_meta.y;

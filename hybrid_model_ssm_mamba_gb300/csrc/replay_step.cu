@@ -159,12 +159,13 @@ replay_step_prep_kernel(StoreView sv, const T* __restrict__ B, const T* __restri
   if (overlap) griddep_wait();  // this grid completes after the previous step's kernels
 }
 
-// The state bytes of slabs [slab, slab + nslab) as a per-head kernel reads them: the FP32
+// The state bytes of slabs [slab, slab + nslab) as a per-head kernel reads them: the
 // checkpoint, or the read copy (NVFP4: codes and block scales).
 template <int P, int N, int RC>
 __device__ __forceinline__ void prefetch_slabs(const StoreView& sv, long long slab, int nslab, bool f32) {
-  if (f32) {
-    prefetch_l2(sv.h0 + slab * P * N, nslab * (P * N * 4u));
+  if (f32) {  // the checkpoint (FP32, or FP16)
+    const unsigned esz = sv.ckpt16 ? 2u : 4u;
+    prefetch_l2(reinterpret_cast<const uint8_t*>(sv.h0) + slab * P * N * esz, nslab * (P * N * esz));
   } else if constexpr (RC == REPLAY_RC_NVFP4) {
     prefetch_l2(static_cast<const uint8_t*>(sv.rc) + slab * (P * N / 2), nslab * (P * N / 2u));
     prefetch_l2(sv.bscale + slab * (P * N / kFp4Block), nslab * (P * N / static_cast<unsigned>(kFp4Block)));
@@ -219,7 +220,7 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
     }
   };
   if (f32_first)
-    load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    load_checkpoint<P, N>(sv, slab, warp, lane, hv);
   else
     load_copy();
   float cv[E];
@@ -266,7 +267,7 @@ replay_step_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ 
 
   // ---------------- flush: fold the k records into h0, write it once, read y from it
   // (from the FP32 checkpoint; a shared copy is the checkpoint and is already loaded)
-  if (!f32_first && !sv.shared) load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+  if (!f32_first && !sv.shared) load_checkpoint<P, N>(sv, slab, warp, lane, hv);
   float* sm_u = reinterpret_cast<float*>(smem4);  // [k][P]: w_s x_s
   float* sm_b = sm_u + cap * P;                   // [k][N]: B_s
   auto b_of = [&](int s) { return s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo; };
@@ -328,7 +329,7 @@ __device__ __noinline__ void copy_read_flush(const StoreView& sv, const T* __res
           for (int e = 0; e < VEC; ++e) hv[i][v * VEC + e] = w[e];
         }
     } else {
-      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+      load_checkpoint<P, N>(sv, slab, warp, lane, hv);
     }
     const float gam = cf[cap];
 #pragma unroll
@@ -569,9 +570,9 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
     return;
   }
 
-  // flush: h <- Gamma h + sum_s w_s x_s B_s^T, HR of the warp's rows at a time
+  // flush: h <- Gamma h + sum_s w_s x_s B_s^T, HR of the warp's rows at a time; each group of
+  // HR rows is reduced and written before the next (fewer live registers: no spills)
   const float gam = cf[cap];
-  float part[RPW];
 #pragma unroll
   for (int hf = 0; hf < RPW / HR; ++hf) {
     const int r0 = warp * RPW + hf * HR;
@@ -607,6 +608,7 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
           hv[i][e + 1] = r.y;
         }
     }
+    float part[HR];
 #pragma unroll
     for (int i = 0; i < HR; ++i) {
       float hc = 0.f;
@@ -620,11 +622,14 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
         }
         stv_stream<VEC>(h0 + (r0 + i) * N + TL::col(lane, v), t);
       }
-      part[hf * HR + i] = hc;
+      part[i] = hc;
+    }
+    const float sum = warp_transpose_reduce<HR>(part, lane);
+    if (transpose_leader<HR>(lane)) {
+      const int row = r0 + transpose_index<HR>(lane);
+      y[xo + row] = fmaf(Dh, to_f(x[xo + row]), sum);
     }
   }
-  const float sum = warp_transpose_reduce<RPW>(part, lane);
-  if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -748,7 +753,7 @@ replay_step_copy_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
           for (int e = 0; e < VEC; ++e) hv[i][v * VEC + e] = w[e];
         }
     } else {
-      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+      load_checkpoint<P, N>(sv, slab, warp, lane, hv);
     }
     auto x_of = [&](int s) { return s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P : x + xo; };
     auto b_of = [&](int s) { return s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo; };
@@ -1004,7 +1009,7 @@ replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restric
     if (sv.shared)
       load_tile_rc<P, N, REPLAY_RC_NVFP4>(sv.rc, slab, sv.scale[slab], warp, lane, hv, sv.bscale);
     else
-      load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+      load_checkpoint<P, N>(sv, slab, warp, lane, hv);
     auto x_of = [&](int s) { return s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P : x + xo; };
     auto b_of = [&](int s) { return s < n ? ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N : B + bo; };
     if (hh > 0) __syncthreads();  // the previous head's staging has been read
@@ -1102,7 +1107,7 @@ replay_step_fused_kernel(StoreView sv, const T* __restrict__ x, const T* __restr
 
   if (flush) {
     if constexpr (RC != REPLAY_RC_NONE) {
-      if (!sv.shared) load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+      if (!sv.shared) load_checkpoint<P, N>(sv, slab, warp, lane, hv);
     }
     float* sm_u = fold_staging(smem4, whole_image_bytes<P, N, T>(cap));
     fold_tile<P, N, T>(im, slot_of, k, A, sm_u, sm_u + cap * P, s_w, hv);
@@ -1241,6 +1246,10 @@ static int launch(const StoreView& base, int all_n, int parity, int overlap, con
 
 int launch_step(const StoreView& sv, const Shape& sh, int all_n, int parity, int overlap, const void* x,
                 const void* B, const void* C, const void* dt, float* y, cudaStream_t stream) {
+  if (step_runs_prep(sv) && step_streams(sv, sh, all_n, dt)) {
+    const int rc = launch_step_stream(sv, sh, x, B, C, dt, y, stream);
+    if (rc != REPLAY_EUNSUPPORTED) return rc;
+  }
 #define RSSM_STEP(NN, TT, RCC)                                                  \
   if (sh.N == NN && sh.in_dtype == RSSM_DTYPE_OF(TT) && sh.read_copy == RCC)    \
     return launch<64, NN, TT, RCC>(sv, all_n, parity, overlap, x, B, C, dt, y, stream);

@@ -193,9 +193,9 @@ replay_verify_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __r
   const float* cf = sv.coef + static_cast<size_t>(slab) * (sv.tmax + 1) * cs;
   const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
 
-  if (prefold) {  // a flush of the committed records, from the FP32 checkpoint
+  if (prefold) {  // a flush of the committed records, from the checkpoint
     if constexpr (RC != REPLAY_RC_NONE) {
-      if (!sv.shared) load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+      if (!sv.shared) load_checkpoint<P, N>(sv, slab, warp, lane, hv);
     }
     float* sm_u = reinterpret_cast<float*>(smem4);
     float* sm_b = sm_u + cap * P;

@@ -20,7 +20,7 @@ from . import build as _build
 __all__ = [
     "ReplayError", "ReplayConfig", "ReplayLayout", "load_library", "header_functions",
     "REPLAY_F32", "REPLAY_BF16", "REPLAY_RC_NONE", "REPLAY_RC_BF16", "REPLAY_RC_FP8E4M3", "REPLAY_RC_FP16",
-    "REPLAY_RC_NVFP4",
+    "REPLAY_RC_NVFP4", "REPLAY_CKPT_F32", "REPLAY_CKPT_F16_SR",
     "REPLAY_DEV_BAD_META", "REPLAY_DEV_BAD_ACCEPT", "REPLAY_DEV_COPY_TIMEOUT",
     "replay_layout_of", "replay_store_bytes", "replay_alloc", "replay_free", "replay_reset",
     "replay_load_state", "replay_export_state", "replay_step", "replay_verify",
@@ -32,6 +32,7 @@ HEADER = pathlib.Path(__file__).resolve().parent.parent / "include" / "replayssm
 
 REPLAY_F32, REPLAY_BF16 = 0, 1
 REPLAY_RC_NONE, REPLAY_RC_BF16, REPLAY_RC_FP8E4M3, REPLAY_RC_FP16, REPLAY_RC_NVFP4 = 0, 1, 2, 3, 4
+REPLAY_CKPT_F32, REPLAY_CKPT_F16_SR = 0, 1
 REPLAY_DEV_BAD_META, REPLAY_DEV_BAD_ACCEPT, REPLAY_DEV_COPY_TIMEOUT = 1, 2, 4
 REPLAY_STATIC_MAX_BATCH = 4096
 REPLAY_STATIC_MAX_COEFS = 1048576
@@ -48,12 +49,13 @@ class ReplayError(RuntimeError):
 class ReplayConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "batch", "nheads", "headdim", "dstate", "ngroups", "window_L", "max_draft_T",
-        "in_dtype", "read_copy", "shared_checkpoint")]
+        "in_dtype", "read_copy", "shared_checkpoint", "checkpoint_format")]
 
     def __init__(self, batch, nheads, headdim, dstate, ngroups, window_L=16, max_draft_T=0,
-                 in_dtype=REPLAY_F32, read_copy=REPLAY_RC_NONE, shared_checkpoint=0):
+                 in_dtype=REPLAY_F32, read_copy=REPLAY_RC_NONE, shared_checkpoint=0,
+                 checkpoint_format=0):
         super().__init__(batch, nheads, headdim, dstate, ngroups, window_L, max_draft_T,
-                         in_dtype, read_copy, shared_checkpoint)
+                         in_dtype, read_copy, shared_checkpoint, checkpoint_format)
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -290,7 +292,8 @@ class ReplayStore:
         Bz, H, P, N, G, cap = c.batch, c.nheads, c.headdim, c.dstate, c.ngroups, L.cap
         dt = self.in_dtype
         spec = {
-            "h0": (torch.float32, (0,) if c.shared_checkpoint else (Bz, H, P, N)),
+            "h0": (torch.float16 if c.checkpoint_format == REPLAY_CKPT_F16_SR else torch.float32,
+                   (0,) if c.shared_checkpoint else (Bz, H, P, N)),
             "rc": ({REPLAY_RC_BF16: torch.bfloat16, REPLAY_RC_FP8E4M3: torch.uint8,
                     REPLAY_RC_FP16: torch.float16}.get(c.read_copy, torch.uint8),
                    (Bz, H, P, N // 2) if c.read_copy == REPLAY_RC_NVFP4 else

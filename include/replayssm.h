@@ -51,8 +51,10 @@ extern "C" {
 #endif
 
 /* 3: the workspace holds two step plans and at least two coefficient blocks (replay_layout
- * sizes changed); status bit REPLAY_DEV_COPY_TIMEOUT. */
-#define REPLAY_ABI_VERSION 3
+ * sizes changed); status bit REPLAY_DEV_COPY_TIMEOUT.
+ * 4: replay_config.checkpoint_format (an FP16 checkpoint with stochastic rounding beside a
+ * separate read copy). */
+#define REPLAY_ABI_VERSION 4
 
 /* element types of x, B, C, dt and of the ring records */
 #define REPLAY_F32 0
@@ -68,10 +70,11 @@ extern "C" {
                               * stochastic rounding named in the post's section "State
                               * quantization". The draw for element e (row-major in P x N) of
                               * slab s = b*H + h, written by the sequence's flush number `epoch`
-                              * (meta.w), is output (epoch*batch*H + s)*P*N + e of the splitmix64
-                              * generator seeded 0x2545F4914F6CDD1D; its top 24 bits over 2^24
-                              * give u, and the value rounds away from zero iff u is below its
-                              * distance from the lower neighbour over the neighbours' spacing.
+                              * (meta.w), is number d = (epoch*batch*H + s)*P*N + e: the 16-bit
+                              * chunk d mod 4 (most significant first) of output d / 4 of the
+                              * splitmix64 generator seeded 0x2545F4914F6CDD1D; u = chunk / 2^16,
+                              * and the value rounds away from zero iff u is below its distance
+                              * from the lower neighbour over the neighbours' spacing.
                               * dstate 64 and 128 only. */
 #define REPLAY_RC_NVFP4 4    /* NVFP4: E2M1 codes, one E4M3 scale per 16 consecutive elements of
                               * a row, one FP32 scale per (b, h) slab: s_g = absmax / 2688 (1 if
@@ -86,6 +89,16 @@ extern "C" {
                               * sign in bit 7 and magnitude in bits 3..1, slot B the sign in bit
                               * 0 and magnitude in bits 6..4 (E2M1 code = sign * 8 + magnitude).
                               * Block scales are [P][N/16] row-major. */
+
+/* format of the recurrence checkpoint (replay_config.checkpoint_format) */
+#define REPLAY_CKPT_F32 0     /* FP32 */
+#define REPLAY_CKPT_F16_SR 1  /* IEEE binary16 written by stochastic rounding (the draws and the
+                               * rounding of REPLAY_RC_FP16 as a shared checkpoint, numbered by
+                               * the same epoch), with a separate read copy cast independently
+                               * from the same FP32 values: the FP16 recurrence with NVFP4 (or
+                               * bf16, E4M3) reads of the post's sections "Benefit 3" and "State
+                               * quantization". Needs read_copy BF16, FP8E4M3 or NVFP4,
+                               * shared_checkpoint 0, dstate <= 128. */
 
 /* host return codes */
 #define REPLAY_OK 0
@@ -116,10 +129,13 @@ typedef struct replay_config {
                           * start from it and write only it, no FP32 checkpoint is kept (the
                           * "shared" low-precision checkpoint the pages compare against: rounded
                           * once per window, and fed back). Needs read_copy != REPLAY_RC_NONE. */
+  int checkpoint_format; /* REPLAY_CKPT_F32 (0) or REPLAY_CKPT_F16_SR: the recurrence checkpoint
+                          * h0 is kept in FP16, rounded stochastically at every write; flushes
+                          * start from it, and non-flush steps and verify read the read copy. */
 } replay_config;
 
 /* Byte offsets of the regions inside the caller's workspace (each 256-byte aligned).
- *   h0     FP32 checkpoint            [batch][H][P][N]
+ *   h0     FP32 checkpoint            [batch][H][P][N]      (FP16 with REPLAY_CKPT_F16_SR)
  *   rc     read copy (bf16/E4M3/FP16) [batch][H][P][N]      (0 bytes without a copy)
  *          NVFP4 codes                [batch][H][P][N/2] bytes (row layout: REPLAY_RC_NVFP4)
  *   scale  FP32 slab scale            [batch][H]            (E4M3 and NVFP4 only)

@@ -203,10 +203,13 @@ def fp16_sr_encode(v, u) -> np.ndarray:
     return np.where(np.asarray(u, dtype=np.float64) < frac, hi, lo).astype(np.uint16)
 
 
-# The random draws of stochastic rounding: value idx of the splitmix64 sequence (Steele,
-# Lea and Flood, OOPSLA 2014) started at SR_SEED, reduced to its top 24 bits: u = z >> 40,
-# u / 2**24 in [0, 1). For the checkpoint of slab `slab` (of `num_slabs`) written by flush
-# number `epoch`, element `elem` of P*N uses idx = (epoch * num_slabs + slab) * (P*N) + elem.
+# The random draws of stochastic rounding, 16 bits each, four per output of the splitmix64
+# sequence (Steele, Lea and Flood, OOPSLA 2014) started at SR_SEED: draw idx is 16-bit chunk
+# idx mod 4 of output idx // 4, the most significant chunk first, and u = chunk / 2**16 in
+# [0, 1). For the checkpoint of slab `slab` (of `num_slabs`) written by flush number `epoch`,
+# element `elem` of P*N takes draw idx = (epoch * num_slabs + slab) * (P*N) + elem. Sixteen
+# bits are exact for every FP16 normal: there the fraction of the spacing is a multiple of
+# 2**-13, so P(u < frac) = frac.
 SR_SEED = 0x2545F4914F6CDD1D
 _SM_GAMMA, _SM_M1, _SM_M2 = 0x9E3779B97F4A7C15, 0xBF58476D1CE4E5B9, 0x94D049BB133111EB
 
@@ -221,8 +224,11 @@ def splitmix64(seed: int, idx) -> np.ndarray:
 
 
 def sr_uniform(idx) -> np.ndarray:
-    """u in [0, 1) (multiples of 2**-24) for draw indices idx (uint64)."""
-    return (splitmix64(SR_SEED, idx) >> np.uint64(40)).astype(np.float64) * 2.0 ** -24
+    """u in [0, 1) (multiples of 2**-16) for draw indices idx (uint64)."""
+    idx = np.asarray(idx, dtype=np.uint64)
+    z = splitmix64(SR_SEED, idx // np.uint64(4))
+    shift = np.uint64(48) - np.uint64(16) * (idx % np.uint64(4))
+    return ((z >> shift) & np.uint64(0xFFFF)).astype(np.float64) * 2.0 ** -16
 
 
 def fp16_sr_round_state(h, epoch: int, slabs, num_slabs: int) -> np.ndarray:

@@ -12,7 +12,7 @@ def test_exports_every_header_symbol(lib):
     assert len(names) >= 17
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.replay_abi_version() == 3
+    assert lib.replay_abi_version() == 4
     assert lib.replay_strerror(-3) == b"capacity exceeded"
 
 
@@ -112,3 +112,22 @@ def test_shared_checkpoint_layout_and_rules():
         with pytest.raises(R.ReplayError) as e:
             R.replay_layout_of(cfg)
         assert e.value.code == -1
+
+
+def test_fp16_checkpoint_layout_and_rules():
+    """checkpoint_format = REPLAY_CKPT_F16_SR keeps the recurrence checkpoint in FP16 (half the
+    bytes) beside a separate read copy; it needs a bf16, E4M3 or NVFP4 copy, no shared
+    checkpoint, and dstate <= 128."""
+    cfg = R.ReplayConfig(4, 8, 64, 128, 4, 16, 0, R.REPLAY_F32, R.REPLAY_RC_NVFP4, 0, R.REPLAY_CKPT_F16_SR)
+    L = R.replay_layout_of(cfg)
+    assert L.h0 == 0 and L.rc == 4 * 8 * 64 * 128 * 2
+    for rc, shared, fmt, code in ((R.REPLAY_RC_NONE, 0, 1, -1), (R.REPLAY_RC_FP16, 0, 1, -1),
+                                  (R.REPLAY_RC_NVFP4, 1, 1, -1), (R.REPLAY_RC_BF16, 0, 2, -1)):
+        bad = R.ReplayConfig(4, 8, 64, 128, 4, 16, 0, R.REPLAY_F32, rc, shared, fmt)
+        with pytest.raises(R.ReplayError) as e:
+            R.replay_layout_of(bad)
+        assert e.value.code == code
+    wide = R.ReplayConfig(4, 8, 64, 256, 4, 16, 0, R.REPLAY_F32, R.REPLAY_RC_BF16, 0, R.REPLAY_CKPT_F16_SR)
+    with pytest.raises(R.ReplayError) as e:
+        R.replay_layout_of(wide)
+    assert e.value.code == -2

@@ -107,14 +107,49 @@ def test_nvfp4_codes_match_format_definition(shared):
         assert np.array_equal(out.cpu().numpy(), _oracle_copy(h)[3].astype(np.float32))
 
 
-# (batch, heads, groups): the fused kernel (batch * heads <= 1024); the NVFP4 tensor-core
-# kernel (heads per group a multiple of 8); the one-head-per-CTA kernel (6 heads per group). A flush the
+def test_nvfp4_codes_at_rounding_boundaries():
+    """Every block holds its maximum and fifteen elements placed within a few ulps of E2M1
+    midpoints (and of the 0.25 boundary) times the block's scale unit e, both signs; block
+    maxima vary so that e is rarely a power of two. Codes, block scales and slab scales equal
+    the encoder's, bit for bit."""
+    shape = sg.LayerShape(1, 2, 64, 128, 1, "f32")
+    st, _, _ = _store(shape, 9, 4)
+    rng = np.random.default_rng(13)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    h = np.empty((1, 2, 64, 128), np.float32)
+    for hh, amax in enumerate((2688.0 * 0.731, 2688.0 * 3.3e-3)):
+        sg_ = np.float32(np.float32(amax) / np.float32(2688.0))
+        blocks = h[0, hh].reshape(-1, 16)
+        for j, blk in enumerate(blocks):
+            bm = np.float32(amax if j == 0 else amax * rng.uniform(0.05, 1.0))
+            sb = F.e4m3_encode(np.float32(bm / np.float32(6.0 * sg_)))
+            e = np.float32(F.e4m3_decode(sb)) * sg_
+            blk[0] = bm
+            for i in range(1, 16):
+                m, k, sgn = mids[(i + j) % 7], (i * 7 + j) % 11 - 5, 1 if (i + j) % 2 else -1
+                blk[i] = sgn * _near(np.float32(m) * np.float32(e), k)
+            blk[1:] = np.clip(blk[1:], -bm, bm)
+    st.load_state(torch.from_numpy(h).cuda())
+    _assert_copy_is_encoding_of(st, h, np.arange(1))
+
+
+def _near(v, k):
+    """FP32 values k ulps from v (k < 0: toward zero)."""
+    v = np.float32(v)
+    for _ in range(abs(k)):
+        v = np.nextafter(v, np.float32(np.inf) if (k > 0) == (v > 0) else np.float32(0))
+    return v
+
+
+# (batch, heads, groups): the fused kernel (batch * heads <= 1024); the streaming kernel when the
+# host knows no sequence flushes (units of 4 heads), else the NVFP4 tensor-core kernel (heads per
+# group a multiple of 8); the one-head-per-CTA kernel (6 heads per group). A flush the
 # host sees coming takes the one-head-per-CTA kernel; after a masked reset (here of no
 # sequence) the host no longer knows the ring counts and every step takes the read kernel,
 # flushes included.
 @pytest.mark.parametrize("batch,heads,groups,dtype,known", [
     (4, 8, 1, "f32", True), (72, 128, 8, "bf16", True), (72, 128, 8, "bf16", False),
-    (96, 12, 2, "f32", True), (96, 12, 2, "f32", False)])
+    (96, 12, 2, "f32", True), (96, 12, 2, "f32", False), (17, 64, 8, "bf16", True), (23, 64, 4, "f32", True)])
 def test_nvfp4_reads_and_flushes_follow_the_oracle(batch, heads, groups, dtype, known):
     shape = sg.LayerShape(batch, heads, 64, 128, groups, dtype)
     L, seed = 8, 23

@@ -302,6 +302,41 @@ def test_read_copy_codes_match_format_definitions(rc, shared):
                 assert same.all(), (b, hh, np.argwhere(~same)[:3])
 
 
+def _near(v, k):
+    """FP32 values k ulps from v (k < 0: toward zero)."""
+    v = np.float32(v)
+    for _ in range(abs(k)):
+        v = np.nextafter(v, np.float32(np.inf) if (k > 0) == (v > 0) else np.float32(0))
+    return v
+
+
+def test_e4m3_codes_at_rounding_boundaries():
+    """Elements placed within a few ulps of every E4M3 midpoint (times a slab scale that is
+    not a power of two, so the quotient is rounded), on both sides and with both signs: the
+    codes still equal the encoder applied to the IEEE FP32 quotient, bit for bit."""
+    shape = sg.LayerShape(1, 2, 64, 128, 1, "f32")
+    A, D = sg.head_params(2, 9)
+    cfg = R.ReplayConfig(1, 2, 64, 128, 1, 4, 0, R.REPLAY_F32, R.REPLAY_RC_FP8E4M3)
+    st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
+    rng = np.random.default_rng(12)
+    h = (rng.standard_normal((1, 2, 64, 128)) * 0.01).astype(np.float32)
+    grid = F.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (grid[:-1] + grid[1:]) / 2                            # every boundary, subnormals included
+    for hh, amax in enumerate((448.0 * 1.3711, 448.0 * 0.0173)):
+        flat = h[0, hh].reshape(-1)
+        flat[0] = amax
+        scale = np.float32(np.float32(amax) / np.float32(448.0))
+        vals = [_near(np.float32(m) * scale, k) * sgn for m in mids for k in range(-5, 6) for sgn in (1, -1)]
+        flat[1:1 + len(vals)] = vals
+    st.load_state(torch.from_numpy(h).cuda())
+    got = st.region("rc").cpu().numpy()
+    for hh in range(2):
+        q, s = F.fp8_slab_quantize(h[0, hh])
+        assert np.float32(st.region("scale").cpu().numpy()[0, hh]) == s
+        same = (got[0, hh] == q) | ((got[0, hh] & 0x7F) == 0) & ((q & 0x7F) == 0)
+        assert same.all(), (hh, np.argwhere(~same)[:3])
+
+
 def test_verify_commit_matches_oracle():
     """Speculative verify + commit with accept ~ U{0..T}, interleaved with decode steps:
     every verify output and the final state match an oracle that decodes only the
@@ -495,13 +530,16 @@ _BF, _F16, _E4 = R.REPLAY_RC_BF16, R.REPLAY_RC_FP16, R.REPLAY_RC_FP8E4M3
     (_BF, 4, 8, 2, "f32", 128), (_F16, 4, 8, 2, "f32", 128), (_E4, 4, 8, 2, "f32", 128),
     (_BF, 72, 128, 8, "bf16", 128), (_F16, 72, 128, 8, "bf16", 128), (_E4, 72, 128, 8, "bf16", 128),
     (_BF, 40, 32, 4, "bf16", 64), (_F16, 40, 32, 4, "f32", 64), (_E4, 40, 32, 4, "bf16", 64),
-    (_BF, 40, 32, 4, "f32", 256), (_E4, 40, 32, 4, "bf16", 256)])
+    (_BF, 40, 32, 4, "f32", 256), (_E4, 40, 32, 4, "bf16", 256),
+    (_BF, 17, 64, 8, "bf16", 128), (_E4, 17, 64, 8, "f32", 128), (_F16, 19, 56, 7, "bf16", 128)])
 def test_copy_reads_follow_the_decoded_copy(rc, batch, heads, groups, dtype, dstate):
     """Non-flush outputs against the unrolled window evaluated in FP64 from the copy's own
     values (the format's decoding of the loaded FP32 state), within 1e-4: the copy is read
     exactly, whichever kernel reads it. Small calls take the fused kernel; calls of more than
-    1024 slabs take the bulk-copy several-heads kernel (2 heads per CTA at dstate 128, 4 at
-    64, 2 for E4M3 at 256) or, for a bf16 copy at dstate 256, the one-head-per-CTA kernel."""
+    1024 slabs at dstate 128 take the streaming kernel (units of 1, 2 heads; here also unit
+    counts that do not split evenly over the SMs), at dstate 64 and 256 the bulk-copy
+    several-heads kernel (4 heads per CTA at 64, 2 for E4M3 at 256) or, for a bf16 copy at
+    dstate 256, the one-head-per-CTA kernel."""
     shape = sg.LayerShape(batch, heads, 64, dstate, groups, dtype)
     L, seed = 8, 31
     st, A, D = make_store(shape, seed, L=L, read_copy=rc)
@@ -578,4 +616,68 @@ def test_shared_checkpoint_matches_periodic_rounding(rc, tol, batch, heads, grou
     d = np.abs(hg[sel] - rounded.h) / np.abs(rounded.h).max(axis=(2, 3), keepdims=True)
     assert d.max() <= 2 * step and (d > 1e-5).mean() <= 1e-3, (d.max(), (d > 1e-5).mean())
     assert e_round <= tol and e_plain > 2 * e_round, (e_round, e_plain)
+    assert st.status() == 0
+
+
+def _decoded_nvfp4(st, seqs):
+    """The values non-flush steps read from the store's NVFP4 copy, decoded from the device's
+    own codes, block scales and slab scales by the oracle's decoder."""
+    q = device_codes(st.region("rc").cpu().numpy()[seqs])
+    sb, sgl = st.region("bscale").cpu().numpy()[seqs], st.region("scale").cpu().numpy()[seqs]
+    out = np.empty(q.shape)
+    for i in np.ndindex(*q.shape[:2]):
+        out[i] = F.nvfp4_slab_dequantize(q[i], sb[i], sgl[i])
+    return out
+
+
+@pytest.mark.parametrize("batch,heads,groups,dtype", [(4, 8, 2, "f32"), (72, 128, 8, "bf16")])
+def test_fp16_sr_checkpoint_with_nvfp4_reads(batch, heads, groups, dtype):
+    """The recurrence checkpoint in FP16 with stochastic rounding, and a separate NVFP4 read
+    copy cast from the same FP32 fold (post, "Benefit 3": NVFP4 reads with an FP16 recurrence).
+    Checked: flush outputs and the FP16 checkpoints follow the oracle that rounds its state
+    stochastically after every window, with the same draws (up to rare flips between FP32 and
+    FP64 states); non-flush outputs equal the window evaluated in FP64 from the device's
+    decoded NVFP4 copy, within 1e-4; the copy is the NVFP4 encoding of the flush's unrounded
+    state (up to the same rare flips), not of the FP16 checkpoint."""
+    shape = sg.LayerShape(batch, heads, 64, 128, groups, dtype)
+    L, steps, seed = 8, 24, 27
+    A, D = sg.head_params(heads, seed)
+    cfg = R.ReplayConfig(batch, heads, 64, 128, groups, L, 0, DTYPE[dtype], R.REPLAY_RC_NVFP4, 0,
+                         R.REPLAY_CKPT_F16_SR)
+    st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
+    sel = np.array([0, batch - 1])
+    A64, D64 = A.astype(float), D.astype(float)
+    z = np.zeros((2, heads, 64, 128))
+    rounded = Mamba2Decoder(A64, D64, groups, z, window_round=_SrRounder(sel, batch * heads), window_L=L)
+    pre = Mamba2Decoder(A64, D64, groups, z.copy())       # the unrounded state within a window
+    y = torch.empty(batch, heads, 64, device="cuda")
+    rec = {k: [] for k in ("x", "B", "dt")}
+    hread = np.zeros((2, heads, 64, 128))
+    e_read = e_flush = 0.0
+    for t in range(steps):
+        devs, f64 = step_inputs(shape, seed, t, sel)
+        st.step(*devs, y)
+        yr = rounded.step(*f64)
+        pre.step(*f64)
+        yg = y[sel].cpu().numpy()
+        for k, v in zip(("x", "B", "dt"), (f64[0], f64[1], f64[3])):
+            rec[k].append(v)
+        if (t + 1) % L:
+            ywin = window_output(hread, np.stack(rec["x"], 1), np.stack(rec["B"], 1), np.stack(rec["dt"], 1),
+                                 f64[2], A64, D64)
+            e_read = max(e_read, rel_vec_err(yg, ywin, 2).max())
+            continue
+        e_flush = max(e_flush, rel_vec_err(yg, yr, 2).max())
+        h16 = st.region("h0").float().cpu().numpy()[sel]
+        d = np.abs(h16 - rounded.h) / np.abs(rounded.h).max(axis=(2, 3), keepdims=True)
+        assert d.max() <= 2 * 2.0 ** -10 and (d > 1e-5).mean() <= 1e-3, (t, d.max(), (d > 1e-5).mean())
+        hread = _decoded_nvfp4(st, sel)
+        want = np.stack([F.nvfp4_round_state(pre.h[i:i + 1])[0] for i in range(2)])
+        flips = np.abs(hread - want) > 1e-6 * np.abs(want).max()
+        assert flips.mean() <= 1e-3, (t, flips.mean())
+        from_ckpt = F.nvfp4_round_state(h16)
+        assert np.abs(hread - from_ckpt).max() > 0                 # cast from FP32, not from FP16
+        pre = Mamba2Decoder(A64, D64, groups, rounded.h.copy())   # the next window starts from it
+        rec = {k: [] for k in ("x", "B", "dt")}
+    assert e_read <= TOL and e_flush <= 1e-3, (e_read, e_flush)
     assert st.status() == 0

@@ -147,10 +147,13 @@ def test_fp16_stochastic_rounding_definition():
 
 
 def test_splitmix64_reference_values():
-    """The first outputs of the published generator started at 0."""
+    """The first outputs of the published generator started at 0, and the 16-bit draws cut
+    from them, most significant chunk first."""
     z = F.splitmix64(0, np.arange(3))
     assert [int(v) for v in z] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
-    assert F.sr_uniform(np.array([5]))[0] == (int(F.splitmix64(F.SR_SEED, [5])[0]) >> 40) / 2.0 ** 24
+    w = int(F.splitmix64(F.SR_SEED, [1])[0])                 # the output that draws 4..7 come from
+    got = F.sr_uniform(np.arange(4, 8, dtype=np.uint64)) * 2.0 ** 16
+    assert got.tolist() == [(w >> 48) & 0xFFFF, (w >> 32) & 0xFFFF, (w >> 16) & 0xFFFF, w & 0xFFFF]
 
 
 # ------------------------------------------------------------------ NVFP4

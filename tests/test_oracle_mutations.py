@@ -152,6 +152,12 @@ def _sr_local_slab(e, s, n, pn, elem, bsz, H):      # slabs numbered within the 
     return (e * n + local) * pn + elem
 
 
+def _sr_chunks_low_first(idx):
+    idx = np.asarray(idx, dtype=np.uint64)
+    z = fm.splitmix64(fm.SR_SEED, idx // np.uint64(4))
+    return ((z >> (np.uint64(16) * (idx % np.uint64(4)))) & np.uint64(0xFFFF)).astype(np.float64) * 2.0 ** -16
+
+
 def _nvfp4_state_blocks_down_columns(h):
     h32 = np.asarray(h, dtype=np.float64).astype(np.float32)
     out = np.empty(h32.shape, dtype=np.float64)
@@ -177,6 +183,7 @@ FORMAT_MUTATIONS = {
     "sr_index_epoch_off_by_one": (
         "fp16_sr_round_state", _sr_state(lambda e, s, n, pn, elem, bsz, H: ((e + np.uint64(1)) * n + s) * pn + elem)),
     "sr_index_subset_numbering_ignored": ("fp16_sr_round_state", _sr_state(_sr_local_slab)),
+    "sr_draw_chunks_low_first": ("sr_uniform", _sr_chunks_low_first),
     "nvfp4_state_blocks_down_columns": ("nvfp4_round_state", _nvfp4_state_blocks_down_columns),
     "nvfp4_state_one_scale_for_all_slabs": ("nvfp4_round_state", _nvfp4_state_one_scale),
 }
