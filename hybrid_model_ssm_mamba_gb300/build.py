@@ -19,7 +19,7 @@ CSRC = PKG / "csrc"
 INCLUDE = PKG.parent / "include"
 LIBDIR = PKG / "lib"
 LIBNAME = "libreplayssm.so"
-SOURCES = ["abi.cu", "replay_step.cu", "replay_stream.cu", "replay_verify.cu", "replay_state.cu", "conv.cu",
+SOURCES = ["abi.cu", "replay_step.cu", "replay_verify.cu", "replay_state.cu", "conv.cu",
            "replay_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

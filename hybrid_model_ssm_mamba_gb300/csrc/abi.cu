@@ -213,9 +213,8 @@ int replay_step(replay_store* st, const void* x, const void* B, const void* C, c
   const int parity = st->sv.prep_appends ? st->step_parity : 0;
   const int rc = rssm::launch_step(st->sv, st->sh, all_n, parity, st->prev_nonflush, x, B, C, dt, y,
                                    as_stream(stream));
-  // (a step run by the streaming kernel has no prep for the next step's prep to follow)
   st->prev_nonflush = rc == REPLAY_OK && st->sv.prep_appends && all_n >= 0 && all_n + 1 < st->cfg.window_L &&
-                      rssm::step_runs_prep(st->sv) && !rssm::step_streams(st->sv, st->sh, all_n, dt);
+                      rssm::step_runs_prep(st->sv);
   if (rc == REPLAY_OK) {
     st->all_n = advance_all_n(st);
     st->step_parity ^= 1;

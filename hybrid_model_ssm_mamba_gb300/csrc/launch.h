@@ -38,12 +38,6 @@ struct Shape {
 int launch_step(const StoreView& sv, const Shape& sh, int all_n, int parity, int overlap, const void* x,
                 const void* B, const void* C, const void* dt, float* y, cudaStream_t stream);
 
-// A step of a read-copy store the host knows flushes no sequence, at dstate 128, runs one
-// persistent kernel that streams the copy (replay_stream.cu) when the shapes allow it.
-bool step_streams(const StoreView& sv, const Shape& sh, int all_n, const void* dt);
-int launch_step_stream(const StoreView& sv, const Shape& sh, const void* x, const void* B, const void* C,
-                       const void* dt, float* y, cudaStream_t stream);
-
 // Calls with at most this many (sequence, head) slabs take the fused step kernel (no prep).
 constexpr long long kFusedMaxSlabs = 1024;
 inline bool step_runs_prep(const StoreView& sv) { return static_cast<long long>(sv.batch) * sv.H > kFusedMaxSlabs; }

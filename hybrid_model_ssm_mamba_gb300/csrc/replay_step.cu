@@ -1246,10 +1246,6 @@ static int launch(const StoreView& base, int all_n, int parity, int overlap, con
 
 int launch_step(const StoreView& sv, const Shape& sh, int all_n, int parity, int overlap, const void* x,
                 const void* B, const void* C, const void* dt, float* y, cudaStream_t stream) {
-  if (step_runs_prep(sv) && step_streams(sv, sh, all_n, dt)) {
-    const int rc = launch_step_stream(sv, sh, x, B, C, dt, y, stream);
-    if (rc != REPLAY_EUNSUPPORTED) return rc;
-  }
 #define RSSM_STEP(NN, TT, RCC)                                                  \
   if (sh.N == NN && sh.in_dtype == RSSM_DTYPE_OF(TT) && sh.read_copy == RCC)    \
     return launch<64, NN, TT, RCC>(sv, all_n, parity, overlap, x, B, C, dt, y, stream);

@@ -141,9 +141,8 @@ def _near(v, k):
     return v
 
 
-# (batch, heads, groups): the fused kernel (batch * heads <= 1024); the streaming kernel when the
-# host knows no sequence flushes (units of 4 heads), else the NVFP4 tensor-core kernel (heads per
-# group a multiple of 8); the one-head-per-CTA kernel (6 heads per group). A flush the
+# (batch, heads, groups): the fused kernel (batch * heads <= 1024); the NVFP4 tensor-core kernel
+# (heads per group a multiple of 8); the one-head-per-CTA kernel (6 heads per group). A flush the
 # host sees coming takes the one-head-per-CTA kernel; after a masked reset (here of no
 # sequence) the host no longer knows the ring counts and every step takes the read kernel,
 # flushes included.

@@ -536,9 +536,8 @@ def test_copy_reads_follow_the_decoded_copy(rc, batch, heads, groups, dtype, dst
     """Non-flush outputs against the unrolled window evaluated in FP64 from the copy's own
     values (the format's decoding of the loaded FP32 state), within 1e-4: the copy is read
     exactly, whichever kernel reads it. Small calls take the fused kernel; calls of more than
-    1024 slabs at dstate 128 take the streaming kernel (units of 1, 2 heads; here also unit
-    counts that do not split evenly over the SMs), at dstate 64 and 256 the bulk-copy
-    several-heads kernel (4 heads per CTA at 64, 2 for E4M3 at 256) or, for a bf16 copy at
+    1024 slabs take the bulk-copy several-heads kernel (2 heads per CTA at dstate 128, 4 at
+    64, 2 for E4M3 at 256; here also group sizes of 7 and 8 heads) or, for a bf16 copy at
     dstate 256, the one-head-per-CTA kernel."""
     shape = sg.LayerShape(batch, heads, 64, dstate, groups, dtype)
     L, seed = 8, 31
