@@ -363,6 +363,14 @@ def run_replay(args, rank, world, local_rank):
             v["nonflush_speedup_vs_fp32"] = fp32_nf_us / v["nonflush_launch_us"]
             v["window_speedup_vs_fp32"] = fp32_window_us / v["window_us"]
         extra["speculative"] = run_speculative(torch, R)
+        # the batch x window sweep of the small layer (fewer tokens than --sweep) and the
+        # 40-layer stack, compact: speed-up of replay over the conventional step per config
+        sw = run_sweep(torch, R, tokens=128)
+        extra["sweep"] = {"workload": "tiny-layer shape (8 heads, FP32 inputs), L2 flushed before every token; "
+                                      "speedup = conventional us / replay us per token",
+                          "speedup": {f"b{r['batch']}_L{r['window_L']}": round(r["speedup"], 3)
+                                      for r in sw if "batch" in r},
+                          "stack_40_layers": {k: v for k, v in sw[-1].items() if k != "sweep"}}
 
     result = {
         "metric": METRIC, "value": tokens / elapsed_max, "unit": UNIT, "n_gpus": world,
@@ -530,7 +538,7 @@ def run_read_copies(torch, R, dev, steps=10):
     return out
 
 
-def run_sweep(torch, R, tokens=512, distinct=32):
+def run_sweep(torch, R, tokens=512, distinct=32, batches=(1, 16, 64, 256, 512), windows=(4, 8, 16, 32)):
     """Batch x window sweep on the tiny layer's shape (8 heads, FP32 inputs), replay vs the
     conventional step, L2 flushed before every token (each token timed alone), plus a
     40-layer stack at batch 256 (2.5 GiB of state, no flush needed). One JSON line each."""
@@ -556,7 +564,7 @@ def run_sweep(torch, R, tokens=512, distinct=32):
         torch.cuda.synchronize()
         return float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3
 
-    for b in (1, 16, 64, 256, 512):
+    for b in batches:
         ins = inputs(b)
         y = torch.empty(b, 8, 64, device="cuda")
         state = torch.zeros(b, 8, 64, 128, device="cuda")
@@ -565,7 +573,7 @@ def run_sweep(torch, R, tokens=512, distinct=32):
         conv = lambda t: R.conv_step(cfg0, state, R.REPLAY_F32, Ad, Dd, *ins[t % distinct], y)  # noqa: E731
         conv(0)
         c_us = per_token_us(conv, tokens)
-        for L in (4, 8, 16, 32):
+        for L in windows:
             cfg = R.ReplayConfig(b, 8, 64, 128, 1, L, 0, R.REPLAY_F32, R.REPLAY_RC_NONE)
             st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
             step = lambda t: st.step(*ins[t % distinct], y)  # noqa: E731
@@ -602,13 +610,37 @@ def run_sweep(torch, R, tokens=512, distinct=32):
     r_stack = timed_stack(lambda t: [s.step(*ins[t % distinct], y) for s in stores], 64)
     c_stack = timed_stack(lambda t: [R.conv_step(cfg, s, R.REPLAY_F32, Ad, Dd, *ins[t % distinct], y)
                                      for s in states], 64)
+    # The same stack with every token's 40 layer steps replayed from a CUDA graph (one graph per
+    # window position for the replay arm, whose kernels depend on the position; one per token
+    # of the window for the conventional arm), so the host's launch rate no longer bounds it.
+    r_graphs, c_graphs = [], []
+    for t in range(L):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for s in stores:
+                s.step(*ins[t % distinct], y)
+        r_graphs.append(g)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for s in states:
+                R.conv_step(cfg, s, R.REPLAY_F32, Ad, Dd, *ins[t % distinct], y)
+        c_graphs.append(g)
+    r_graph = timed_stack(lambda t: r_graphs[t % L].replay(), 64)
+    c_graph = timed_stack(lambda t: c_graphs[t % L].replay(), 64)
+    layer_bytes = sum(step_bytes(dict(batch=b, nheads=8, headdim=64, dstate=128, ngroups=1), t, t == L - 1, esz=4)
+                      for t in range(L)) / L
     for s in stores:
         assert s.status() == 0
         s.close()
     out.append({"sweep": "40-layer stack, tiny-layer shape, batch 256, L 16 (2.5 GiB of state)",
                 "replay_us_per_token_all_layers": r_stack, "conv_us_per_token_all_layers": c_stack,
                 "replay_tokens_per_s": b / (r_stack * 1e-6), "conv_tokens_per_s": b / (c_stack * 1e-6),
-                "speedup": c_stack / r_stack})
+                "speedup": c_stack / r_stack,
+                "graph_replay_us_per_token": r_graph, "graph_conv_us_per_token": c_graph,
+                "graph_speedup": c_graph / r_graph,
+                "graph_replay_achieved_gbs": layers * layer_bytes / (r_graph * 1e-6) / 1e9,
+                "graph_conv_achieved_gbs": layers * conv_bytes(dict(batch=b, nheads=8, headdim=64, dstate=128,
+                                                                     ngroups=1), esz=4) / (c_graph * 1e-6) / 1e9})
     return out
 
 

@@ -313,7 +313,7 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   unsigned* s_bf = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(s_cf) +
                                                align128(static_cast<size_t>(TT) * (cap + 1) * sizeof(float)));
   const int NG = (TT + 3) / 4;
-  T* s_rec = reinterpret_cast<T*>(s_bf + NG * 16 * 32 * 2);  // [n2][P] committed records' x
+  T* s_rec = reinterpret_cast<T*>(s_bf + NG * 16 * 32 * 2);  // [cap][P] this head's x ring, by slot
 
   // Independent of the prep kernel: the lane's 32 checkpoint values, the drafts' C and x in
   // shared memory, and each thread's share of the drafts' records to append (x of this
@@ -335,6 +335,12 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
     }
   }
   cp_async_commit();
+  // This head's whole x ring, by slot: its committed records are among them whatever the
+  // ring pointer turns out to be, and the prep does not write them, so the copy need not wait
+  // for the plan (the slots past the committed records are copied for nothing).
+  const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+  for (int c = tid; c < cap * XC; c += kThreads) cp_async16(s_rec + c * EPC, ring.x + c * EPC);
+  cp_async_commit();
   const int nxc = TT * XC, nbc = blockIdx.x == 0 ? TT * BC : 0, napp = nxc + nbc + TT;
   uint4 app[2];
   T appdt[2];
@@ -354,6 +360,10 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   const float Dh = sv.D[h];
 
   griddep_wait();  // plan and coefficients of this call are written
+  // the plan and this thread's share of the drafts' coefficients in one round trip
+  const int cs = cap + 1;
+  const float* cf = sv.coef + static_cast<size_t>(slab) * (sv.tmax + 1) * cs;
+  const float cfv = tid < TT * cs ? cf[cs + tid] : 0.f;
   const int4 pl = sv.plan[b];
   if (pl.z == kVerifyBad) {
     cp_async_wait_all();
@@ -365,15 +375,6 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   const bool prefold = pl.z == kVerifyPrefold;
   const int start2 = prefold ? ring_slot(start, n, cap) : start;
   const int n2 = prefold ? 0 : n;
-  const int cs = cap + 1;
-  const float* cf = sv.coef + static_cast<size_t>(slab) * (sv.tmax + 1) * cs;
-  const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
-  // the committed records the drafts see (a pre-fold folds them first: then there are none)
-  for (int c = tid; c < n2 * XC; c += kThreads) {
-    const int s = c / XC, off = (c - s * XC) * EPC;
-    cp_async16(s_rec + s * P + off, ring.x + static_cast<size_t>(ring_slot(start2, s, cap)) * P + off);
-  }
-  cp_async_commit();
   // the drafts' records go to the ring beyond the committed ones; the pointer stays
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -412,7 +413,8 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   }
 
   // coefficients and B fragments (the drafts' C, split) into shared memory
-  for (int i = tid; i < TT * cs; i += kThreads) s_cf[i] = cf[cs + i];
+  if (tid < TT * cs) s_cf[tid] = cfv;
+  for (int i = tid + kThreads; i < TT * cs; i += kThreads) s_cf[i] = cf[cs + i];
   cp_async_wait_group<1>();  // the drafts' C and x
   __syncthreads();
   for (int e = tid; e < NG * 16 * 32 * 2; e += kThreads) {
@@ -423,7 +425,7 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
     const float c = j < TT ? to_f(sq[j * N + col]) : 0.f;
     s_bf[e] = (gg >> 2) ? tf32_lo(c) : tf32_hi(c);
   }
-  cp_async_wait_all();  // the committed records
+  cp_async_wait_all();  // the x ring
   __syncthreads();
 
   // d[set]: the MMA accumulators of drafts 4 set .. 4 set + 3
@@ -457,7 +459,7 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
       const float hc = (q >> 1) ? d1 : d0;
       const float* cj = s_cf + j * cs;
       float ex = 0.f;  // records draft j sees: the n2 committed ones, then drafts 0..j
-      for (int s = 0; s < n2; ++s) ex = fmaf(cj[s], to_f(s_rec[s * P + row]), ex);
+      for (int s = 0; s < n2; ++s) ex = fmaf(cj[s], to_f(s_rec[ring_slot(start2, s, cap) * P + row]), ex);
       for (int s = 0; s <= j; ++s) ex = fmaf(cj[n2 + s], to_f(sx[s * P + row]), ex);
       yb[static_cast<size_t>(j) * H * P + row] = fmaf(Dh, to_f(sx[j * P + row]), fmaf(cj[cap], hc, ex));
     }
