@@ -774,13 +774,15 @@ replay_step_copy_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
 // NVFP4 copy (dstate 128). A slab's copy is 4 KiB of codes and 512 B of block scales, so a CTA
 // takes 8 heads of a group, one warp per head. h0 . C of a head is a 64 x 128 by 128 product,
 // done on the tensor cores with mma.sync m16n8k16 (f16 inputs, FP32 accumulation): one MMA
-// per (16-row tile, block), its k dimension one NVFP4 block, so the block scale applies to
-// its result. The codes become FP16 operands with integer ops only: slot A of a stored byte
-// is already the high byte of the FP16 value * 2^-14, slot B takes two shifts, and a byte
-// permute with zero places two codes in an FP16 pair. C enters as the B operand split into an
-// FP16 high and low part (columns 0 and 1; the other six columns are zero), after scaling the
+// per (16-row tile, block), its k dimension one NVFP4 block. The codes become FP16 operands
+// with integer ops only: slot A of a stored byte is already the high byte of the FP16 value *
+// 2^-14, slot B takes two shifts, and a byte permute with zero places two codes in an FP16
+// pair. C enters as the B operand split into an FP16 high and low part, after scaling the
 // group's C by a power of two that brings its largest value to [2^13, 2^14): the products are
-// exact in FP32 and C keeps about 22 bits. Lane (g, q) = (lane / 4, lane % 4) reads quarter q
+// exact in FP32 and C keeps about 22 bits. Block bk's MMA puts the two parts in columns
+// 2 (bk mod 4) and 2 (bk mod 4) + 1, so each block's unscaled sum lands in a column pair of its
+// own and the block scale weights it once per (row, block) afterwards (scaling every operand
+// pair cost as many instructions as the decode). Lane (g, q) = (lane / 4, lane % 4) reads quarter q
 // of rows g and g + 8 of every 16-row tile (one 16-byte load each) and holds the A fragment
 // columns of that quarter; the MMA k index 2q, 2q+1, 2q+8, 2q+9 is block column 4q .. 4q+3.
 // d += a b
@@ -807,21 +809,6 @@ template <int I>
 __device__ __forceinline__ unsigned fp4_pair(unsigned x) {
   return prmt(x, 0u, 4u | (I << 4) | (4u << 8) | ((I + 1) << 12));
 }
-// Two E4M3 block scales (bytes I and I + 1 of w) as an FP16 pair: a code's 7 magnitude bits
-// placed at bits 13..7 of an FP16 are its value times 2^-8 (subnormal codes included, as FP16
-// subnormals), so one exact multiply by 256 restores it.
-template <int I>
-__device__ __forceinline__ __half2 fp16_scale_pair(unsigned w) {
-  const unsigned t = (prmt(w, 0u, I | (4u << 4) | ((I + 1) << 8) | (4u << 12)) << 7) & 0x3F803F80u;
-  return __hmul2(*reinterpret_cast<const __half2*>(&t), __float2half2_rn(256.f));
-}
-// An FP16 pair times one FP16 scale (exact here: a code times a scale has at most 6
-// significant bits and stays a multiple of 2^-24 below 1).
-__device__ __forceinline__ unsigned scale_pair(unsigned p, __half s) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&p), __half2half2(s));
-  return *reinterpret_cast<const unsigned*>(&r);
-}
-
 // Dynamic shared memory of the NVFP4 kernel: per warp (head) its codes and block scales,
 // staged by cp.async before the prep wait, then its k records (x) staged after it.
 template <int P, int N, class T>
@@ -891,12 +878,16 @@ replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restric
     s_ch[tid / N][cc] = tid < N ? hi : __float2half_rn(cs - __half2float(hi));
   }
   __syncthreads();
+  // B operand of block bk's MMA: C's high part in column 2 (bk mod 4), its low part in column
+  // 2 (bk mod 4) + 1, zero elsewhere; lane (gq, q) holds column gq.
   unsigned bf[NB][2];
 #pragma unroll
   for (int bk = 0; bk < NB; ++bk)
 #pragma unroll
     for (int j = 0; j < 2; ++j)
-      bf[bk][j] = gq < 2 ? *reinterpret_cast<const unsigned*>(&s_ch[gq][bk * kFp4Block + 4 * q + 2 * j]) : 0u;
+      bf[bk][j] = (gq >> 1) == (bk & 3)
+                      ? *reinterpret_cast<const unsigned*>(&s_ch[gq & 1][bk * kFp4Block + 4 * q + 2 * j])
+                      : 0u;
   const float xk0 = to_f(x[xow + lane]), xk1 = to_f(x[xow + lane + 32]);
 
   griddep_wait();  // plan and coefficients of this step are written
@@ -928,41 +919,43 @@ replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restric
     const float gsc = cf[cap] * sv.scale[slabw] * down;
     cp_async_wait_group<1>();  // the codes and scales (the records may still be in flight)
     __syncwarp();
-    // h0 . C: rows gq and gq + 8 of each tile end up in the lanes with q == 0
+    // h0 . C: each block's MMA takes its codes unscaled (FP16 pairs placed by integer ops) and
+    // writes its sum over the block's 16 columns into columns 2 (bk mod 4) and 2 (bk mod 4) + 1
+    // (C high, low) of accumulator bk / 4; the block scales then weight the 8 block sums of a row
+    // once each. Rows gq and gq + 8 of each tile end up in the lanes with q == 0.
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int r0 = mt * 16 + gq;
       const uint4 W0 = *reinterpret_cast<const uint4*>(s_codes + fp4_unit(r0, 0, q));
       const uint4 W1 = *reinterpret_cast<const uint4*>(s_codes + fp4_unit(r0 + 8, 0, q));
-      const uint2 S0 = *reinterpret_cast<const uint2*>(s_scales + r0 * NB);
-      const uint2 S1 = *reinterpret_cast<const uint2*>(s_scales + (r0 + 8) * NB);
-      // The A operands carry their block scale (the MMAs then accumulate over the blocks).
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int wd = 0; wd < 4; ++wd) {  // word wd holds blocks 2 wd and 2 wd + 1
         const unsigned w0 = wd == 0 ? W0.x : wd == 1 ? W0.y : wd == 2 ? W0.z : W0.w;
         const unsigned w1 = wd == 0 ? W1.x : wd == 1 ? W1.y : wd == 2 ? W1.z : W1.w;
-        const unsigned sw0 = wd < 2 ? S0.x : S0.y, sw1 = wd < 2 ? S1.x : S1.y;
-        const __half2 sc0 = (wd & 1) ? fp16_scale_pair<2>(sw0) : fp16_scale_pair<0>(sw0);  // row gq
-        const __half2 sc1 = (wd & 1) ? fp16_scale_pair<2>(sw1) : fp16_scale_pair<0>(sw1);  // row gq + 8
         const unsigned a0 = fp4_placed_a(w0), b0 = fp4_placed_b(w0);
         const unsigned a1 = fp4_placed_a(w1), b1 = fp4_placed_b(w1);
-        {
-          const int bk = 2 * wd;
-          const __half s0 = __low2half(sc0), s1 = __low2half(sc1);
-          mma_16816(acc, scale_pair(fp4_pair<0>(a0), s0), scale_pair(fp4_pair<0>(a1), s1),
-                    scale_pair(fp4_pair<0>(b0), s0), scale_pair(fp4_pair<0>(b1), s1), bf[bk][0], bf[bk][1]);
-        }
-        {
-          const int bk = 2 * wd + 1;
-          const __half s0 = __high2half(sc0), s1 = __high2half(sc1);
-          mma_16816(acc, scale_pair(fp4_pair<2>(a0), s0), scale_pair(fp4_pair<2>(a1), s1),
-                    scale_pair(fp4_pair<2>(b0), s0), scale_pair(fp4_pair<2>(b1), s1), bf[bk][0], bf[bk][1]);
-        }
+        mma_16816(acc[wd >> 1], fp4_pair<0>(a0), fp4_pair<0>(a1), fp4_pair<0>(b0), fp4_pair<0>(b1), bf[2 * wd][0],
+                  bf[2 * wd][1]);
+        mma_16816(acc[wd >> 1], fp4_pair<2>(a0), fp4_pair<2>(a1), fp4_pair<2>(b0), fp4_pair<2>(b1),
+                  bf[2 * wd + 1][0], bf[2 * wd + 1][1]);
       }
+      // lane (gq, q): blocks q and q + 4 of rows gq and gq + 8, high plus low part
+      const float za0 = acc[0][0] + acc[0][1], za1 = acc[1][0] + acc[1][1];
+      const float zb0 = acc[0][2] + acc[0][3], zb1 = acc[1][2] + acc[1][3];
+      // their block scales (E4M3 bytes q and q + 4 of the rows' scale words), as FP32
+      const uint2 S0 = *reinterpret_cast<const uint2*>(s_scales + r0 * NB);
+      const uint2 S1 = *reinterpret_cast<const uint2*>(s_scales + (r0 + 8) * NB);
+      const float2 sa = e4m3x2_to_float2(static_cast<unsigned short>(prmt(S0.x, S0.y, q | ((q + 4) << 4))));
+      const float2 sb = e4m3x2_to_float2(static_cast<unsigned short>(prmt(S1.x, S1.y, q | ((q + 4) << 4))));
+      float ta = fmaf(za1, sa.y, za0 * sa.x), tb = fmaf(zb1, sb.y, zb0 * sb.x);
+      ta += __shfl_xor_sync(kFull, ta, 1);
+      tb += __shfl_xor_sync(kFull, tb, 1);
+      ta += __shfl_xor_sync(kFull, ta, 2);
+      tb += __shfl_xor_sync(kFull, tb, 2);
       if (q == 0) {
-        s_y[warp][mt * 16 + gq] = acc[0] + acc[1];
-        s_y[warp][mt * 16 + gq + 8] = acc[2] + acc[3];
+        s_y[warp][mt * 16 + gq] = ta;
+        s_y[warp][mt * 16 + gq + 8] = tb;
       }
     }
     cp_async_wait_all();
