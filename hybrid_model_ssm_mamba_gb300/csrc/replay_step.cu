@@ -818,7 +818,7 @@ constexpr size_t fp4_stage_bytes(int heads, int cap) {
 }
 
 template <int P, int N, class T, int HPC>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
 replay_step_fp4_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
                        const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
   static_assert(P == 64 && N == 128 && HPC == kWarps && 2 * N == kThreads, "one warp per head, 64 x 128 slabs");
@@ -1208,9 +1208,14 @@ static int launch(const StoreView& base, int all_n, int parity, int overlap, con
   if constexpr (RC == REPLAY_RC_NVFP4 && N == 128) {
     constexpr int HPC = 8;
     const size_t fsmem = std::max(smem, fp4_stage_bytes<P, N, T>(HPC, sv.cap));
-    if (!all_flush && sv.hpg % HPC == 0)
+    if (!all_flush && sv.hpg % HPC == 0) {
+      // 4 CTAs of 52 KB share an SM only with the largest shared-memory carveout
+      static const cudaError_t carveout = cudaFuncSetAttribute(
+          replay_step_fp4_kernel<P, N, T, HPC>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      (void)carveout;
       return pdl_launch(replay_step_fp4_kernel<P, N, T, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch), fsmem, stream,
                         sv, tx, tB, tC, tdt, y);
+    }
   } else if constexpr (RC != REPLAY_RC_NONE && RC != REPLAY_RC_NVFP4) {
     constexpr int HPC = heads_per_cta<N, RC>();
     // the bulk-copy kernel takes at most 2 heads of E4M3 at dstate 128 (16 KB): 6 CTAs per SM
