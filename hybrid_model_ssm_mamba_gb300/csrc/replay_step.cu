@@ -1209,10 +1209,11 @@ static int launch(const StoreView& base, int all_n, int parity, int overlap, con
     constexpr int HPC = 8;
     const size_t fsmem = std::max(smem, fp4_stage_bytes<P, N, T>(HPC, sv.cap));
     if (!all_flush && sv.hpg % HPC == 0) {
-      // 4 CTAs of 52 KB share an SM only with the largest shared-memory carveout
-      static const cudaError_t carveout = cudaFuncSetAttribute(
-          replay_step_fp4_kernel<P, N, T, HPC>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-      (void)carveout;
+      // 4 CTAs of 52 KB share an SM only with the largest shared-memory carveout (a preference:
+      // set on the current device before every launch, like the dynamic shared-memory size)
+      if (cudaFuncSetAttribute(replay_step_fp4_kernel<P, N, T, HPC>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               100) != cudaSuccess)
+        return REPLAY_ECUDA;
       return pdl_launch(replay_step_fp4_kernel<P, N, T, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch), fsmem, stream,
                         sv, tx, tB, tC, tdt, y);
     }
