@@ -446,58 +446,67 @@ __device__ __forceinline__ void load_tile_rc(const void* rc, size_t slab, float 
     }
 }
 
+// One row of a copy tile: the lane's E values of row `row` (columns Tile::col(lane, v)).
+template <int P, int N, int RC>
+__device__ __forceinline__ void store_row_rc(void* rc, size_t slab, float scale, int row, int lane,
+                                             const float (&vals)[Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+#pragma unroll
+  for (int v = 0; v < TL::NVEC; ++v) {
+    float t[TL::VEC];
+#pragma unroll
+    for (int e = 0; e < TL::VEC; ++e) t[e] = vals[v * TL::VEC + e];
+    const size_t off = slab * P * N + static_cast<size_t>(row) * N + TL::col(lane, v);
+    if constexpr (RC == REPLAY_RC_BF16)
+      st_bf16_stream<TL::VEC>(static_cast<bf16*>(rc) + off, t);
+    else if constexpr (RC == REPLAY_RC_FP16)
+      st_f16_stream<TL::VEC>(static_cast<__half*>(rc) + off, t);
+    else
+      st_e4m3_stream<TL::VEC>(static_cast<uint8_t*>(rc) + off, scale, t);
+  }
+}
+
 template <int P, int N, int RC>
 __device__ __forceinline__ void store_tile_rc(void* rc, size_t slab, float scale, int warp, int lane,
                                               const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
   using TL = Tile<P, N>;
 #pragma unroll
-  for (int i = 0; i < TL::RPW; ++i)
-#pragma unroll
-    for (int v = 0; v < TL::NVEC; ++v) {
-      float t[TL::VEC];
-#pragma unroll
-      for (int e = 0; e < TL::VEC; ++e) t[e] = hv[i][v * TL::VEC + e];
-      const size_t off = slab * P * N + TL::row(warp, i) * N + TL::col(lane, v);
-      if constexpr (RC == REPLAY_RC_BF16)
-        st_bf16_stream<TL::VEC>(static_cast<bf16*>(rc) + off, t);
-      else if constexpr (RC == REPLAY_RC_FP16)
-        st_f16_stream<TL::VEC>(static_cast<__half*>(rc) + off, t);
-      else
-        st_e4m3_stream<TL::VEC>(static_cast<uint8_t*>(rc) + off, scale, t);
-    }
+  for (int i = 0; i < TL::RPW; ++i) store_row_rc<P, N, RC>(rc, slab, scale, TL::row(warp, i), lane, hv[i]);
 }
 
-// An NVFP4 tile with slab scale sg: each 16-element block of a row (4 consecutive lanes)
+// An NVFP4 row with slab scale sg: each 16-element block of the row (4 consecutive lanes)
 // takes s_b = e4m3(block absmax / (6 sg)) and codes e2m1(h / (s_b sg)), every step one FP32
 // operation; a block whose scale is 0 stores zero codes. Lane l's 4 columns are the unit of
-// block l / 4, quarter l % 4 (layout above).
+// block l / 4, quarter l % 4 (layout above). The whole warp calls it (block maxima by shuffles).
+template <int P, int N>
+__device__ __forceinline__ void store_row_nvfp4(void* rc, uint8_t* bscale, size_t slab, float sg, int row, int lane,
+                                                const float (&t)[Tile<P, N>::E]) {
+  static_assert(N == 128 && Tile<P, N>::E == 4, "the NVFP4 copy is laid out for dstate 128");
+  const float unit = __fmul_rn(kE2M1Max, sg);
+  float bm = fmaxf(fmaxf(fabsf(t[0]), fabsf(t[1])), fmaxf(fabsf(t[2]), fabsf(t[3])));
+  bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+  bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+  const unsigned int sb = float2_to_e4m3x2(__fdiv_rn(bm, unit), 0.f) & 0xffu;
+  const float es = __fmul_rn(e4m3_to_float(sb), sg);
+  unsigned int c01 = 0, c23 = 0;  // E2M1 codes of columns (0, 1) and (2, 3), low nibble first
+  if (es > 0.f) {
+    c01 = float2_to_e2m1x2(__fdiv_rn(t[0], es), __fdiv_rn(t[1], es));
+    c23 = float2_to_e2m1x2(__fdiv_rn(t[2], es), __fdiv_rn(t[3], es));
+  }
+  const unsigned int b0 = fp4_slot_a(c01 & 15u) | fp4_slot_b(c23 & 15u);
+  const unsigned int b1 = fp4_slot_a(c01 >> 4) | fp4_slot_b(c23 >> 4);
+  __stcs(reinterpret_cast<unsigned short*>(static_cast<uint8_t*>(rc) + slab * P * N / 2 +
+                                           fp4_unit(row, lane >> 2, lane & 3)),
+         static_cast<unsigned short>(b0 | (b1 << 8)));
+  if ((lane & 3) == 0) __stcs(bscale + (slab * P + row) * (N / kFp4Block) + (lane >> 2), static_cast<uint8_t>(sb));
+}
+
 template <int P, int N>
 __device__ __forceinline__ void store_tile_nvfp4(void* rc, uint8_t* bscale, size_t slab, float sg, int warp,
                                                  int lane, const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
   using TL = Tile<P, N>;
-  static_assert(N == 128 && TL::VEC == 4 && TL::NVEC == 1, "the NVFP4 copy is laid out for dstate 128");
-  const float unit = __fmul_rn(kE2M1Max, sg);
 #pragma unroll
-  for (int i = 0; i < TL::RPW; ++i) {
-    const float* t = hv[i];
-    float bm = fmaxf(fmaxf(fabsf(t[0]), fabsf(t[1])), fmaxf(fabsf(t[2]), fabsf(t[3])));
-    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
-    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
-    const unsigned int sb = float2_to_e4m3x2(__fdiv_rn(bm, unit), 0.f) & 0xffu;
-    const float es = __fmul_rn(e4m3_to_float(sb), sg);
-    unsigned int c01 = 0, c23 = 0;  // E2M1 codes of columns (0, 1) and (2, 3), low nibble first
-    if (es > 0.f) {
-      c01 = float2_to_e2m1x2(__fdiv_rn(t[0], es), __fdiv_rn(t[1], es));
-      c23 = float2_to_e2m1x2(__fdiv_rn(t[2], es), __fdiv_rn(t[3], es));
-    }
-    const unsigned int b0 = fp4_slot_a(c01 & 15u) | fp4_slot_b(c23 & 15u);
-    const unsigned int b1 = fp4_slot_a(c01 >> 4) | fp4_slot_b(c23 >> 4);
-    const int row = TL::row(warp, i);
-    __stcs(reinterpret_cast<unsigned short*>(static_cast<uint8_t*>(rc) + slab * P * N / 2 +
-                                             fp4_unit(row, lane >> 2, lane & 3)),
-           static_cast<unsigned short>(b0 | (b1 << 8)));
-    if ((lane & 3) == 0) __stcs(bscale + (slab * P + row) * (N / kFp4Block) + (lane >> 2), static_cast<uint8_t>(sb));
-  }
+  for (int i = 0; i < TL::RPW; ++i) store_row_nvfp4<P, N>(rc, bscale, slab, sg, TL::row(warp, i), lane, hv[i]);
 }
 
 // The same decision with a 16-bit draw u16 (u = u16 / 2^16), in integers for FP16 normals:
@@ -515,38 +524,45 @@ __device__ __forceinline__ unsigned short f16_sr16(float v, unsigned u16) {
   return f16_sr(v, static_cast<float>(u16) * 0x1p-16f);
 }
 
-// An FP16 tile by stochastic rounding: element e of slab `slab` (of num_slabs) written by
-// flush `epoch` takes draw (epoch * num_slabs + slab) * P*N + e. A lane's VEC columns start at
-// a multiple of VEC, so they share one generator output (two lanes share it when VEC is 2).
+// An FP16 row by stochastic rounding: element e of slab `slab` (of num_slabs) written by flush
+// `epoch` takes draw (epoch * num_slabs + slab) * P*N + e. A lane's VEC columns start at a
+// multiple of VEC, so they share one generator output (two lanes share it when VEC is 2).
+template <int P, int N>
+__device__ __forceinline__ void store_row_f16_sr(void* rc, size_t slab, unsigned long long epoch,
+                                                 unsigned long long num_slabs, int row, int lane,
+                                                 const float (&vals)[Tile<P, N>::E]) {
+  using TL = Tile<P, N>;
+  static_assert(TL::VEC == 2 || TL::VEC == 4, "a lane's columns lie within one generator output");
+  const unsigned long long base = (epoch * num_slabs + slab) * static_cast<unsigned long long>(P * N);
+#pragma unroll
+  for (int v = 0; v < TL::NVEC; ++v) {
+    const int e0 = row * N + TL::col(lane, v);
+    const unsigned long long z = splitmix64_at(kSrSeed, (base + e0) >> 2);
+    unsigned short c[TL::VEC];
+#pragma unroll
+    for (int e = 0; e < TL::VEC; ++e) {
+      const int chunk = (e0 + e) & 3;  // base is a multiple of 4
+      c[e] = f16_sr16(vals[v * TL::VEC + e], static_cast<unsigned>(z >> (48 - 16 * chunk)) & 0xffffu);
+    }
+    __half* p = static_cast<__half*>(rc) + slab * P * N + e0;
+    if constexpr (TL::VEC == 4) {
+      uint2 w;
+      w.x = c[0] | (static_cast<unsigned int>(c[1]) << 16);
+      w.y = c[2] | (static_cast<unsigned int>(c[3]) << 16);
+      __stcs(reinterpret_cast<uint2*>(p), w);
+    } else {
+      __stcs(reinterpret_cast<unsigned int*>(p), c[0] | (static_cast<unsigned int>(c[1]) << 16));
+    }
+  }
+}
+
 template <int P, int N>
 __device__ __forceinline__ void store_tile_f16_sr(void* rc, size_t slab, unsigned long long epoch,
                                                   unsigned long long num_slabs, int warp, int lane,
                                                   const float (&hv)[Tile<P, N>::RPW][Tile<P, N>::E]) {
   using TL = Tile<P, N>;
-  static_assert(TL::VEC == 2 || TL::VEC == 4, "a lane's columns lie within one generator output");
-  const unsigned long long base = (epoch * num_slabs + slab) * static_cast<unsigned long long>(P * N);
 #pragma unroll
-  for (int i = 0; i < TL::RPW; ++i)
-#pragma unroll
-    for (int v = 0; v < TL::NVEC; ++v) {
-      const int e0 = TL::row(warp, i) * N + TL::col(lane, v);
-      const unsigned long long z = splitmix64_at(kSrSeed, (base + e0) >> 2);
-      unsigned short c[TL::VEC];
-#pragma unroll
-      for (int e = 0; e < TL::VEC; ++e) {
-        const int chunk = (e0 + e) & 3;  // base is a multiple of 4
-        c[e] = f16_sr16(hv[i][v * TL::VEC + e], static_cast<unsigned>(z >> (48 - 16 * chunk)) & 0xffffu);
-      }
-      __half* p = static_cast<__half*>(rc) + slab * P * N + e0;
-      if constexpr (TL::VEC == 4) {
-        uint2 w;
-        w.x = c[0] | (static_cast<unsigned int>(c[1]) << 16);
-        w.y = c[2] | (static_cast<unsigned int>(c[3]) << 16);
-        __stcs(reinterpret_cast<uint2*>(p), w);
-      } else {
-        __stcs(reinterpret_cast<unsigned int*>(p), c[0] | (static_cast<unsigned int>(c[1]) << 16));
-      }
-    }
+  for (int i = 0; i < TL::RPW; ++i) store_row_f16_sr<P, N>(rc, slab, epoch, num_slabs, TL::row(warp, i), lane, hv[i]);
 }
 
 // ------------------------------------------------------------------ warp reductions

@@ -493,16 +493,55 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
 template <int N, bool FL>
 constexpr int kReadCtas = N >= 256 ? (FL ? 2 : 3) : (FL ? 5 : 6);
 
-template <int P, int N, class T, bool FL>
+// A non-flush plan reaching the flush kernel of a read-copy store (the host expected a flush):
+// the output reads the copy, like every non-flush step of such a store. Out of line.
+template <int P, int N, class T, int RC>
+__device__ __noinline__ void read_copy_nonflush(const StoreView& sv, const T* __restrict__ x,
+                                                const T* __restrict__ C, float* __restrict__ y, int b, int g,
+                                                int h, int start, int n) {
+  using TL = Tile<P, N>;
+  constexpr int RPW = TL::RPW, E = TL::E, EPC = 16 / sizeof(T), XC = P / EPC;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slab = b * sv.H + h, cap = sv.cap, k = n + 1;
+  const size_t xo = static_cast<size_t>(slab) * P;
+  float hv[RPW][E];
+  const float scale = RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4 ? sv.scale[slab] : 1.f;
+  load_tile_rc<P, N, RC>(sv.rc, slab, scale, warp, lane, hv, sv.bscale);
+  float cv[E];
+  load_cols<P, N>(C + (static_cast<size_t>(b) * sv.G + g) * N, lane, cv);
+  const float* cf = sv.coef + static_cast<size_t>(slab) * (cap + 1);
+  const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+  auto x_of = [&](int s) { return s < n ? ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P : x + xo; };
+  float xr[RPW];
+  record_terms<RPW, T>(x_of, cf, k, warp, lane, xr);
+  const float sum = tile_rows_dot<P, N>(hv, cv, cf[cap], xr, lane);
+  const int myrow = warp * RPW + transpose_index<RPW>(lane);
+  if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(sv.D[h], to_f(x[xo + myrow]), sum);
+  if (tid < XC)  // (B and dt: the prep appends them for read-copy stores)
+    *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(ring_slot(start, n, cap)) * P + tid * EPC) =
+        *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
+}
+
+// RC, CK16 (the launch is for a flush, FL): besides the checkpoint, the flush writes the read
+// copy RC of a store whose checkpoint is not the copy. bf16 and FP16 rows are cast as they are
+// folded; an E4M3 or NVFP4 copy needs the slab's absmax first, so the folded rows go back into
+// the shared slab and are encoded from there once the CTA has reduced it. CK16: the checkpoint
+// is FP16 (stochastic rounding, rows written as folded); its slab arrives by the same bulk
+// copy and is widened into the FP32 slab before the fold.
+template <int P, int N, class T, bool FL, int RC = REPLAY_RC_NONE, bool CK16 = false>
 __global__ void __launch_bounds__(kThreads, kReadCtas<N, FL>)
 replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
                         const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
   using TL = Tile<P, N>;
   constexpr int RPW = TL::RPW, E = TL::E, VEC = TL::VEC, NVEC = TL::NVEC, HR = FL ? RPW / 2 : RPW / 4;
   constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
+  constexpr bool ENC = RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4;  // encoded after an absmax
+  static_assert(FL || (RC == REPLAY_RC_NONE && !CK16), "copies are written by the flush launch only");
+  constexpr unsigned CKB = CK16 ? 2u : 4u;  // checkpoint bytes per element
   extern __shared__ float4 smem4[];
   __shared__ __align__(8) unsigned long long s_bar;
   __shared__ int s_landed;
+  __shared__ float s_red[kWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y, b = blockIdx.z;
@@ -512,10 +551,11 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   const size_t xo = static_cast<size_t>(slab) * P;
   const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
   float* s_h = reinterpret_cast<float*>(smem4);
-  float* h0 = sv.h0 + static_cast<size_t>(slab) * P * N;
+  float* h0 = sv.h0 + static_cast<size_t>(slab) * P * N;  // (FP32 checkpoints only)
   if (tid == 0) {
     mbar_init(&s_bar);
-    bulk_load(s_h, h0, P * N * sizeof(float), &s_bar);
+    bulk_load(s_h, reinterpret_cast<const uint8_t*>(sv.h0) + static_cast<size_t>(slab) * P * N * CKB, P * N * CKB,
+              &s_bar);
   }
   if (FL) prefetch_next_wave<P, N, REPLAY_RC_NONE>(sv, slab, 1, kReadCtas<N, FL>, true);
   float cv[E];
@@ -534,11 +574,11 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   float* sm_u = s_h + P * N;     // FL: [k][P] w_s x_s, then [k][N] B_s
   float* sm_b = sm_u + cap * P;
   float xr[RPW];
-  if (pl.z == kPlanNonFlush) record_terms<RPW, T>(x_of, cf, k, warp, lane, xr);
+  if (RC == REPLAY_RC_NONE && pl.z == kPlanNonFlush) record_terms<RPW, T>(x_of, cf, k, warp, lane, xr);
   if (FL && pl.z == kPlanFlush) stage_weighted<P, N, T>(x_of, b_of, cf, k, sm_u, sm_b);
   // The slab must have landed before it is read or the CTA exits; one thread waits, the rest
-  // at the barrier (which also publishes a flush's staging). A copy past its limit leaves this slab's y NaN and its state untouched
-  // (after a second bounded wait).
+  // at the barrier (which also publishes a flush's staging). A copy past its limit leaves this
+  // slab's y NaN and its state untouched (after a second bounded wait).
   if (tid == 0) {
     const bool ok = mbar_wait(&s_bar, 0, kCopyWaitNs);
     if (!ok) {
@@ -554,25 +594,53 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   }
 
   if (pl.z == kPlanNonFlush) {
-    const float sum = smem_rows_dot<P, N>(s_h, cv, cf[cap], xr, warp, lane);
-    if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
-    const int slot = ring_slot(start, n, cap);
-    if (tid < XC) {
-      *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
-          *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
-    } else if (!sv.prep_appends && blockIdx.x == 0 && tid < XC + BC) {  // B once per group
-      const int c = tid - XC;
-      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
-          *reinterpret_cast<const uint4*>(B + bo + c * EPC);
-    } else if (!sv.prep_appends && tid == XC + BC) {
-      ring.dt[slot] = dt[slab];
+    if constexpr (RC != REPLAY_RC_NONE) {
+      read_copy_nonflush<P, N, T, RC>(sv, x, C, y, b, g, h, start, n);
+      return;
+    } else {
+      const float sum = smem_rows_dot<P, N>(s_h, cv, cf[cap], xr, warp, lane);
+      if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
+      const int slot = ring_slot(start, n, cap);
+      if (tid < XC) {
+        *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + tid * EPC) =
+            *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
+      } else if (!sv.prep_appends && blockIdx.x == 0 && tid < XC + BC) {  // B once per group
+        const int c = tid - XC;
+        *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+            *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+      } else if (!sv.prep_appends && tid == XC + BC) {
+        ring.dt[slot] = dt[slab];
+      }
+      return;
     }
-    return;
   }
 
-  // flush: h <- Gamma h + sum_s w_s x_s B_s^T, HR of the warp's rows at a time; each group of
-  // HR rows is reduced and written before the next (fewer live registers: no spills)
+  if constexpr (CK16) {  // widen the FP16 checkpoint in place: read all, barrier, write all
+    const __half* s_h16 = reinterpret_cast<const __half*>(s_h);
+    float wv[RPW][E];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+          wv[i][v * VEC + e] = __half2float(s_h16[TL::row(warp, i) * N + TL::col(lane, v) + e]);
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) s_h[TL::row(warp, i) * N + TL::col(lane, v) + e] = wv[i][v * VEC + e];
+    __syncthreads();
+  }
+
+  // flush: h <- Gamma h + sum_s w_s x_s B_s^T, HR of the warp's rows at a time. The FP32-only
+  // store reduces all of the warp's rows at the end (measured faster than a reduction per group
+  // of HR rows, despite a few spilled bytes); the copy stores reduce each group as it is done.
   const float gam = cf[cap];
+  float amax = 0.f;
+  float partall[RPW];
 #pragma unroll
   for (int hf = 0; hf < RPW / HR; ++hf) {
     const int r0 = warp * RPW + hf * HR;
@@ -613,21 +681,76 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
     for (int i = 0; i < HR; ++i) {
       float hc = 0.f;
 #pragma unroll
-      for (int v = 0; v < NVEC; ++v) {
-        float t[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          t[e] = hv[i][v * VEC + e];
-          hc = fmaf(t[e], cv[v * VEC + e], hc);
-        }
-        stv_stream<VEC>(h0 + (r0 + i) * N + TL::col(lane, v), t);
-      }
+      for (int e = 0; e < E; ++e) hc = fmaf(hv[i][e], cv[e], hc);
       part[i] = hc;
+      if constexpr (CK16) {
+        store_row_f16_sr<P, N>(sv.h0, slab, static_cast<unsigned int>(pl.w),
+                               static_cast<unsigned long long>(sv.batch) * sv.H, r0 + i, lane, hv[i]);
+      } else {
+#pragma unroll
+        for (int v = 0; v < NVEC; ++v) {
+          float t[VEC];
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) t[e] = hv[i][v * VEC + e];
+          stv_stream<VEC>(h0 + (r0 + i) * N + TL::col(lane, v), t);
+        }
+      }
+      if constexpr (RC == REPLAY_RC_BF16 || RC == REPLAY_RC_FP16) {
+        store_row_rc<P, N, RC>(sv.rc, slab, 1.f, r0 + i, lane, hv[i]);
+      } else if constexpr (ENC) {  // back into the slab, for the encoding below
+#pragma unroll
+        for (int v = 0; v < NVEC; ++v) {
+          float t[VEC];
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            t[e] = hv[i][v * VEC + e];
+            amax = fmaxf(amax, fabsf(t[e]));
+          }
+          *reinterpret_cast<float4*>(s_h + (r0 + i) * N + TL::col(lane, v)) = make_float4(t[0], t[1], t[2], t[3]);
+        }
+      }
     }
-    const float sum = warp_transpose_reduce<HR>(part, lane);
-    if (transpose_leader<HR>(lane)) {
-      const int row = r0 + transpose_index<HR>(lane);
-      y[xo + row] = fmaf(Dh, to_f(x[xo + row]), sum);
+    if constexpr (RC == REPLAY_RC_NONE && !CK16) {
+#pragma unroll
+      for (int i = 0; i < HR; ++i) partall[hf * HR + i] = part[i];
+    } else {
+      const float sum = warp_transpose_reduce<HR>(part, lane);
+      if (transpose_leader<HR>(lane)) {
+        const int row = r0 + transpose_index<HR>(lane);
+        y[xo + row] = fmaf(Dh, to_f(x[xo + row]), sum);
+      }
+    }
+  }
+  if constexpr (RC == REPLAY_RC_NONE && !CK16) {
+    const float sum = warp_transpose_reduce<RPW>(partall, lane);
+    if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
+  }
+  if constexpr (ENC) {
+    // the slab's absmax, its scale, then the codes of the warp's own rows from the slab
+    amax = warp_max(amax);
+    if (lane == 0) s_red[warp] = amax;
+    __syncthreads();
+    float m = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, s_red[w]);
+    const float scale = RC == REPLAY_RC_FP8E4M3 ? (m > 0.f ? __fdiv_rn(m, kE4M3Max) : 1.f)
+                                                : (m > 0.f ? __fdiv_rn(m, kE4M3Max * kE2M1Max) : 1.f);
+    if (tid == 0) sv.scale[slab] = scale;
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      const int row = warp * RPW + i;
+      float t[E];
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v) {
+        float w4[VEC];
+        ldv<VEC>(s_h + row * N + TL::col(lane, v), w4);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) t[v * VEC + e] = w4[e];
+      }
+      if constexpr (RC == REPLAY_RC_FP8E4M3)
+        store_row_rc<P, N, RC>(sv.rc, slab, scale, row, lane, t);
+      else
+        store_row_nvfp4<P, N>(sv.rc, sv.bscale, slab, scale, row, lane, t);
     }
   }
 }
@@ -1217,7 +1340,20 @@ static int launch(const StoreView& base, int all_n, int parity, int overlap, con
       return pdl_launch(replay_step_fp4_kernel<P, N, T, HPC>, dim3(sv.hpg / HPC, sv.G, sv.batch), fsmem, stream,
                         sv, tx, tB, tC, tdt, y);
     }
-  } else if constexpr (RC != REPLAY_RC_NONE && RC != REPLAY_RC_NVFP4) {
+  }
+  if constexpr (RC != REPLAY_RC_NONE && N == 128) {  // a known flush of a copy store: bulk-copy flush kernel
+    const size_t flsmem = static_cast<size_t>(P) * N * sizeof(float) + smem;
+    if (all_flush && !sv.shared) {
+      if constexpr (RC != REPLAY_RC_FP16) {
+        if (sv.ckpt16)
+          return pdl_launch(replay_step_read_kernel<P, N, T, true, RC, true>, dim3(sv.hpg, sv.G, sv.batch), flsmem,
+                            stream, sv, tx, tB, tC, tdt, y);
+      }
+      return pdl_launch(replay_step_read_kernel<P, N, T, true, RC, false>, dim3(sv.hpg, sv.G, sv.batch), flsmem,
+                        stream, sv, tx, tB, tC, tdt, y);
+    }
+  }
+  if constexpr (RC != REPLAY_RC_NONE && RC != REPLAY_RC_NVFP4) {
     constexpr int HPC = heads_per_cta<N, RC>();
     // the bulk-copy kernel takes at most 2 heads of E4M3 at dstate 128 (16 KB): 6 CTAs per SM
     // beat 4 with 4 heads each (measured)
