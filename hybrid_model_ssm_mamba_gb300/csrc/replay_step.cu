@@ -522,13 +522,11 @@ __device__ __noinline__ void read_copy_nonflush(const StoreView& sv, const T* __
         *reinterpret_cast<const uint4*>(x + xo + tid * EPC);
 }
 
-// RC, CK16 (the launch is for a flush, FL): besides the checkpoint, the flush writes the read
-// copy RC of a store whose checkpoint is not the copy. bf16 and FP16 rows are cast as they are
-// folded; an E4M3 or NVFP4 copy needs the slab's absmax first, so the folded rows go back into
-// the shared slab and are encoded from there once the CTA has reduced it. CK16: the checkpoint
-// is FP16 (stochastic rounding, rows written as folded); its slab arrives by the same bulk
-// copy and is widened into the FP32 slab before the fold.
-template <int P, int N, class T, bool FL, int RC = REPLAY_RC_NONE, bool CK16 = false>
+// RC (the launch is for a flush, FL): besides the FP32 checkpoint, the flush writes the read
+// copy RC. bf16 and FP16 rows are cast as they are folded; an E4M3 or NVFP4 copy needs the
+// slab's absmax first, so the folded rows go back into the shared slab and are encoded from
+// there once the CTA has reduced it.
+template <int P, int N, class T, bool FL, int RC = REPLAY_RC_NONE>
 __global__ void __launch_bounds__(kThreads, kReadCtas<N, FL>)
 replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
                         const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
@@ -536,8 +534,7 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   constexpr int RPW = TL::RPW, E = TL::E, VEC = TL::VEC, NVEC = TL::NVEC, HR = FL ? RPW / 2 : RPW / 4;
   constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC;
   constexpr bool ENC = RC == REPLAY_RC_FP8E4M3 || RC == REPLAY_RC_NVFP4;  // encoded after an absmax
-  static_assert(FL || (RC == REPLAY_RC_NONE && !CK16), "copies are written by the flush launch only");
-  constexpr unsigned CKB = CK16 ? 2u : 4u;  // checkpoint bytes per element
+  static_assert(FL || RC == REPLAY_RC_NONE, "copies are written by the flush launch only");
   extern __shared__ float4 smem4[];
   __shared__ __align__(8) unsigned long long s_bar;
   __shared__ int s_landed;
@@ -551,11 +548,10 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
   const size_t xo = static_cast<size_t>(slab) * P;
   const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
   float* s_h = reinterpret_cast<float*>(smem4);
-  float* h0 = sv.h0 + static_cast<size_t>(slab) * P * N;  // (FP32 checkpoints only)
+  float* h0 = sv.h0 + static_cast<size_t>(slab) * P * N;
   if (tid == 0) {
     mbar_init(&s_bar);
-    bulk_load(s_h, reinterpret_cast<const uint8_t*>(sv.h0) + static_cast<size_t>(slab) * P * N * CKB, P * N * CKB,
-              &s_bar);
+    bulk_load(s_h, h0, P * N * sizeof(float), &s_bar);
   }
   if (FL) prefetch_next_wave<P, N, REPLAY_RC_NONE>(sv, slab, 1, kReadCtas<N, FL>, true);
   float cv[E];
@@ -615,26 +611,6 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
     }
   }
 
-  if constexpr (CK16) {  // widen the FP16 checkpoint in place: read all, barrier, write all
-    const __half* s_h16 = reinterpret_cast<const __half*>(s_h);
-    float wv[RPW][E];
-#pragma unroll
-    for (int i = 0; i < RPW; ++i)
-#pragma unroll
-      for (int v = 0; v < NVEC; ++v)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-          wv[i][v * VEC + e] = __half2float(s_h16[TL::row(warp, i) * N + TL::col(lane, v) + e]);
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < RPW; ++i)
-#pragma unroll
-      for (int v = 0; v < NVEC; ++v)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) s_h[TL::row(warp, i) * N + TL::col(lane, v) + e] = wv[i][v * VEC + e];
-    __syncthreads();
-  }
-
   // flush: h <- Gamma h + sum_s w_s x_s B_s^T, HR of the warp's rows at a time. The FP32-only
   // store reduces all of the warp's rows at the end (measured faster than a reduction per group
   // of HR rows, despite a few spilled bytes); the copy stores reduce each group as it is done.
@@ -683,17 +659,12 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
 #pragma unroll
       for (int e = 0; e < E; ++e) hc = fmaf(hv[i][e], cv[e], hc);
       part[i] = hc;
-      if constexpr (CK16) {
-        store_row_f16_sr<P, N>(sv.h0, slab, static_cast<unsigned int>(pl.w),
-                               static_cast<unsigned long long>(sv.batch) * sv.H, r0 + i, lane, hv[i]);
-      } else {
 #pragma unroll
-        for (int v = 0; v < NVEC; ++v) {
-          float t[VEC];
+      for (int v = 0; v < NVEC; ++v) {
+        float t[VEC];
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) t[e] = hv[i][v * VEC + e];
-          stv_stream<VEC>(h0 + (r0 + i) * N + TL::col(lane, v), t);
-        }
+        for (int e = 0; e < VEC; ++e) t[e] = hv[i][v * VEC + e];
+        stv_stream<VEC>(h0 + (r0 + i) * N + TL::col(lane, v), t);
       }
       if constexpr (RC == REPLAY_RC_BF16 || RC == REPLAY_RC_FP16) {
         store_row_rc<P, N, RC>(sv.rc, slab, 1.f, r0 + i, lane, hv[i]);
@@ -710,7 +681,7 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
         }
       }
     }
-    if constexpr (RC == REPLAY_RC_NONE && !CK16) {
+    if constexpr (RC == REPLAY_RC_NONE) {
 #pragma unroll
       for (int i = 0; i < HR; ++i) partall[hf * HR + i] = part[i];
     } else {
@@ -721,7 +692,7 @@ replay_step_read_kernel(StoreView sv, const T* __restrict__ x, const T* __restri
       }
     }
   }
-  if constexpr (RC == REPLAY_RC_NONE && !CK16) {
+  if constexpr (RC == REPLAY_RC_NONE) {
     const float sum = warp_transpose_reduce<RPW>(partall, lane);
     if (transpose_leader<RPW>(lane)) y[xo + myrow] = fmaf(Dh, xk_row, sum);
   }
@@ -1343,15 +1314,11 @@ static int launch(const StoreView& base, int all_n, int parity, int overlap, con
   }
   if constexpr (RC != REPLAY_RC_NONE && N == 128) {  // a known flush of a copy store: bulk-copy flush kernel
     const size_t flsmem = static_cast<size_t>(P) * N * sizeof(float) + smem;
-    if (all_flush && !sv.shared) {
-      if constexpr (RC != REPLAY_RC_FP16) {
-        if (sv.ckpt16)
-          return pdl_launch(replay_step_read_kernel<P, N, T, true, RC, true>, dim3(sv.hpg, sv.G, sv.batch), flsmem,
-                            stream, sv, tx, tB, tC, tdt, y);
-      }
-      return pdl_launch(replay_step_read_kernel<P, N, T, true, RC, false>, dim3(sv.hpg, sv.G, sv.batch), flsmem,
+    // (a shared checkpoint, or an FP16 one, measured faster in the register-tile kernel below:
+    // there the slab read is the small copy, or the stochastic rounding dominates)
+    if (all_flush && !sv.shared && !sv.ckpt16)
+      return pdl_launch(replay_step_read_kernel<P, N, T, true, RC>, dim3(sv.hpg, sv.G, sv.batch), flsmem,
                         stream, sv, tx, tB, tC, tdt, y);
-    }
   }
   if constexpr (RC != REPLAY_RC_NONE && RC != REPLAY_RC_NVFP4) {
     constexpr int HPC = heads_per_cta<N, RC>();
