@@ -423,12 +423,12 @@ def l2_flusher(torch):
     return lambda: buf.fill_(1.0)
 
 
-def run_speculative(torch, R, calls=64, distinct=16):
-    """Speculative verify on the tiny layer's shape at batch 512, T = 4, accept ~ U{0..T}:
+def run_speculative(torch, R, calls=64, distinct=16, T=None):
+    """Speculative verify on the tiny layer's shape at batch 512, T = 4 (or T), accept ~ U{0..T}:
     ReplaySSM verify + commit against snapshot-per-draft verify + commit, and against one
     conventional decode step of the same shape; L2 is flushed before every timed call."""
     w = SPEC
-    T, L = w["T"], w["L"]
+    T, L = T or w["T"], w["L"]
     shape = sg.LayerShape(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["dtype"])
     A, D = sg.head_params(w["nheads"], 0)
     cfg = R.ReplayConfig(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], L, T,
@@ -475,7 +475,7 @@ def run_speculative(torch, R, calls=64, distinct=16):
     r_us, s_us, c_us = timed(replay), timed(snapshot), timed(standard)
     assert st.status() == 0
     st.close()
-    return {"workload": "tiny-layer shape at batch 512, 8 heads, T=4, accept ~ U{0..4}, L2 flushed per call",
+    return {"workload": f"tiny-layer shape at batch 512, 8 heads, T={T}, accept ~ U{{0..{T}}}, L2 flushed per call",
             "replay_verify_commit_us": r_us, "snapshot_verify_commit_us": s_us,
             "conventional_step_us": c_us, "replay_speedup_vs_snapshot": s_us / r_us,
             "snapshot_vs_standard_step": s_us / c_us, "replay_vs_standard_step": r_us / c_us,
@@ -759,6 +759,8 @@ def main(argv=None):
                     help="diagnostics: time only the replay windows and print a short line (for ncu runs)")
     ap.add_argument("--verify-only", action="store_true",
                     help="diagnostics: run only the speculative verify workload and print its line")
+    ap.add_argument("--drafts", type=int, default=0,
+                    help="diagnostics with --verify-only: draft count T (default 4)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line: batch x window sweep and 40-layer stack, "
                          "one JSON line per configuration")
@@ -769,7 +771,7 @@ def main(argv=None):
         import torch
         from hybrid_model_ssm_mamba_gb300 import replay as R
         torch.cuda.set_device(local_rank)
-        lines = run_sweep(torch, R) if args.sweep else [run_speculative(torch, R, calls=args.steps)]
+        lines = run_sweep(torch, R) if args.sweep else [run_speculative(torch, R, calls=args.steps, T=args.drafts)]
         for line in lines:
             print(json.dumps(line), flush=True)
         return
