@@ -38,17 +38,46 @@ template <int P, int N, class T, int kPrepThreads>
 __global__ void __launch_bounds__(kPrepThreads)
 replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T* __restrict__ C,
                           const T* __restrict__ dt) {
-  constexpr int kPrepWarps = kPrepThreads / 32;
-  using TL = Tile<P, N>;
+  constexpr int EPC = 16 / sizeof(T), BC = N / EPC;
   __shared__ int4 s_meta;
   __shared__ float s_bc[kMaxDrafts][kMaxCap];
   __shared__ float s_dt[kDtStage];
+  extern __shared__ float4 smem4[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x, b = blockIdx.y;
-  const int H = sv.H, G = sv.G, cap = sv.cap;
-  auto boff = [&](int j) { return (static_cast<size_t>(b) * TT + j) * G * N + static_cast<size_t>(g) * N; };
+  const int H = sv.H, G = sv.G, cap = sv.cap, hpg = sv.hpg;
   griddep_launch_dependents();  // the head CTAs may start their checkpoint loads now
+
+  // One round trip for everything, the ring pointer included: the group's whole B ring by slot
+  // (the committed records are among its slots wherever the pointer is), the drafts' B and C,
+  // and every head's dt ring by slot beside the drafts' dt.
+  T* sring = reinterpret_cast<T*>(smem4);  // [cap][N] the B ring, by slot
+  T* sdb = sring + static_cast<size_t>(cap) * N;  // [TT][N] the drafts' B
+  T* sdc = sdb + static_cast<size_t>(TT) * N;     // [TT][N] the drafts' C
+  const T* bring = static_cast<const T*>(sv.bbuf) + (static_cast<size_t>(b) * G + g) * cap * N;
   if (tid == 0) s_meta = sv.meta[b];
+  for (int c = tid; c < (cap + 2 * TT) * BC; c += kPrepThreads) {
+    const int r = c / BC, off = (c - r * BC) * EPC;
+    const T* src;
+    if (r < cap) {
+      src = bring + static_cast<size_t>(r) * N;
+    } else {
+      const int j = r < cap + TT ? r - cap : r - cap - TT;
+      src = (r < cap + TT ? B : C) + (static_cast<size_t>(b) * TT + j) * G * N + static_cast<size_t>(g) * N;
+    }
+    cp_async16(sring + static_cast<size_t>(r) * N + off, src + off);
+  }
+  cp_async_commit();
+  // s_dt: [hpg][cap] the heads' dt rings by slot, then [hpg][TT] the drafts' dt
+  const bool stage_dt = hpg * (cap + TT) <= kDtStage;
+  const T* dtring = static_cast<const T*>(sv.dtbuf) + (static_cast<size_t>(b) * H + g * hpg) * cap;
+  if (stage_dt) {
+    for (int i = tid; i < hpg * cap; i += kPrepThreads) s_dt[i] = to_f(dtring[i]);
+    for (int i = tid; i < hpg * TT; i += kPrepThreads) {
+      const int j = i / hpg, hh = i - j * hpg;
+      s_dt[hpg * cap + hh * TT + j] = to_f(dt[(static_cast<size_t>(b) * TT + j) * H + g * hpg + hh]);
+    }
+  }
   __syncthreads();
   const int start = s_meta.x, n = s_meta.y, epoch = s_meta.w;
   if (n < 0 || start < 0 || start >= cap || n + TT > cap) {
@@ -56,6 +85,7 @@ replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T
       if (g == 0) sv.plan[b] = make_int4(start, n, kVerifyBad, epoch);
       set_status(sv.status, REPLAY_DEV_BAD_META);
     }
+    cp_async_wait_all();
     return;
   }
   const bool prefold = n >= sv.L;
@@ -65,71 +95,74 @@ replay_verify_prep_kernel(StoreView sv, int TT, const T* __restrict__ B, const T
     if (g == 0) sv.plan[b] = make_int4(start, n, prefold ? kVerifyPrefold : kVerifyPlain, epoch);
     arrive_and_publish(sv, b, make_int4(start2, n2, TT, epoch + (prefold ? 1 : 0)), G);
   }
-  const T* bring = static_cast<const T*>(sv.bbuf) + (static_cast<size_t>(b) * G + g) * cap * N;
   const int kk = n2 + TT;  // committed records after any pre-fold, then the drafts
-  // every head's dt values -- the pre-folded records', then the queries' records' -- in one
-  // round trip (when they fit), beside the B and C staging below
-  const int nf = prefold ? n : 0, per = nf + kk;
-  const bool stage_dt = sv.hpg * per <= kDtStage;
+  const int nf = prefold ? n : 0;
+  // dt of head hh's record i: the n pre-folded records from start, then the kk query records
   auto dt_rec = [&](int hh, int i) {
-    const size_t slab = static_cast<size_t>(b) * H + g * sv.hpg + hh;
-    const T* dtr = static_cast<const T*>(sv.dtbuf) + slab * cap;
-    if (i < nf) return to_f(dtr[ring_slot(start, i, cap)]);
     const int s = i - nf;
-    return to_f(s < n2 ? dtr[ring_slot(start2, s, cap)]
-                       : dt[(static_cast<size_t>(b) * TT + (s - n2)) * H + g * sv.hpg + hh]);
-  };
-  // stage the kk records' B and the TT queries' C in shared memory by cp.async, and the dt
-  // values meanwhile: one round trip
-  extern __shared__ float4 smem4[];
-  T* sb = reinterpret_cast<T*>(smem4);  // [kk][N] B of the records, then [TT][N] C of the drafts
-  {
-    constexpr int EPC = 16 / sizeof(T), BC = N / EPC;
-    for (int c = tid; c < (kk + TT) * BC; c += kPrepThreads) {
-      const int r = c / BC, off = (c - r * BC) * EPC;
-      const T* src = r >= kk ? C + boff(r - kk)
-                             : (r < n2 ? bring + static_cast<size_t>(ring_slot(start2, r, cap)) * N : B + boff(r - n2));
-      cp_async16(sb + static_cast<size_t>(r) * N + off, src + off);
+    if (i < nf || s < n2) {
+      const int slot = i < nf ? ring_slot(start, i, cap) : ring_slot(start2, s, cap);
+      return stage_dt ? s_dt[hh * cap + slot] : to_f(dtring[hh * cap + slot]);
     }
-    if (stage_dt)
-      for (int idx = tid; idx < sv.hpg * per; idx += kPrepThreads) s_dt[idx] = dt_rec(idx / per, idx % per);
-    cp_async_wait_all();
-    __syncthreads();
-  }
-  for (int pi = warp; pi < TT * kk; pi += kPrepWarps) {
-    const int j = pi / kk, s = pi - j * kk;
+    const int j = s - n2;
+    return stage_dt ? s_dt[hpg * cap + hh * TT + j]
+                    : to_f(dt[(static_cast<size_t>(b) * TT + j) * H + g * hpg + hh]);
+  };
+  cp_async_wait_all();
+  __syncthreads();
+
+  // B_s . C_j for s <= n2 + j, one thread each: a serial sum over the 16-byte chunks, each
+  // thread starting at its own chunk so that a warp's loads fall in distinct banks
+  for (int p = tid; p < TT * kk; p += kPrepThreads) {
+    const int j = p / kk, s = p - j * kk;
     if (s > n2 + j) continue;
-    float bv[TL::E], cj[TL::E];
-    load_cols<P, N>(sb + static_cast<size_t>(s) * N, lane, bv);
-    load_cols<P, N>(sb + static_cast<size_t>(kk + j) * N, lane, cj);
-    float d = 0.f;
+    const T* br = s < n2 ? sring + static_cast<size_t>(ring_slot(start2, s, cap)) * N
+                         : sdb + static_cast<size_t>(s - n2) * N;
+    const T* cr = sdc + static_cast<size_t>(j) * N;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int c = 0; c < BC; ++c) {
+      const int off = ((c + tid) % BC) * EPC;
+      float bv[EPC], cv[EPC];
+      load16(br + off, bv);
+      load16(cr + off, cv);
 #pragma unroll
-    for (int e = 0; e < TL::E; ++e) d = fmaf(bv[e], cj[e], d);
-    d = warp_sum(d);
-    if (lane == 0) s_bc[j][s] = d;
+      for (int e = 0; e < EPC; ++e) acc[e & 3] = fmaf(bv[e], cv[e], acc[e & 3]);
+    }
+    s_bc[j][s] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
   }
   __syncthreads();
+
+  // Per head (one warp each): the fold weights of pre-folded records, then the query
+  // coefficients. With Q_i = sum_{r<i} dt_r over the kk query records (one warp scan), draft j
+  // sees k = n2 + j + 1 records and c_j[s] = exp(A (Q_k - Q_{s+1})) dt_s (B_s . C_j),
+  // Gamma_j = exp(A Q_k).
   const int cs = cap + 1;
-  for (int hh = warp; hh < sv.hpg; hh += kPrepWarps) {
-    const int h = g * sv.hpg + hh;
+  for (int hh = warp; hh < hpg; hh += kPrepThreads / 32) {
+    const int h = g * hpg + hh;
     const size_t slab = static_cast<size_t>(b) * H + h;
     const float A = sv.A[h];
     float* cf = sv.coef + slab * (sv.tmax + 1) * cs;
-    auto dt_at = [&](int i) { return stage_dt ? s_dt[hh * per + i] : dt_rec(hh, i); };
     if (prefold) {
-      auto dt_fold = [&](int s) { return dt_at(s); };
+      auto dt_fold = [&](int s) { return dt_rec(hh, s); };
       write_fold_weights(dt_fold, n, A, cf, cap, lane);
     }
-    auto dt_q = [&](int s) { return dt_at(nf + s); };
-    const float d0 = lane < kk ? dt_q(lane) : 0.f;
-    const float d1 = lane + 32 < kk ? dt_q(lane + 32) : 0.f;
+    const float d0 = lane < kk ? dt_rec(hh, nf + lane) : 0.f;
+    const float d1 = lane + 32 < kk ? dt_rec(hh, nf + lane + 32) : 0.f;
+    float q0 = d0, q1 = d1;  // inclusive prefix sums: Q_{lane+1}, Q_{lane+33}
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float u0 = __shfl_up_sync(kFull, q0, off), u1 = __shfl_up_sync(kFull, q1, off);
+      if (lane >= off) { q0 += u0; q1 += u1; }
+    }
+    q1 += __shfl_sync(kFull, q0, 31);
     for (int j = 0; j < TT; ++j) {
       const int k = n2 + j + 1;
-      const RecordWeights rw = record_weights(lane < k ? d0 : 0.f, lane + 32 < k ? d1 : 0.f, k, A, lane);
+      const float qk = __shfl_sync(kFull, k <= 32 ? q0 : q1, (k - 1) & 31);
       float* cj = cf + (1 + j) * cs;
-      if (lane < k) cj[lane] = rw.w0 * s_bc[j][lane];
-      if (lane + 32 < k) cj[lane + 32] = rw.w1 * s_bc[j][lane + 32];
-      if (lane == 0) cj[cap] = rw.gam;
+      if (lane < k) cj[lane] = __expf(A * (qk - q0)) * d0 * s_bc[j][lane];
+      if (lane + 32 < k) cj[lane + 32] = __expf(A * (qk - q1)) * d1 * s_bc[j][lane + 32];
+      if (lane == 0) cj[cap] = __expf(A * qk);
     }
   }
 }
@@ -285,7 +318,7 @@ constexpr size_t tc_verify_smem(int TT, int cap) {
 }
 
 template <int P, int N, class T>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
 replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __restrict__ B,
                         const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
   static_assert(P == 64 && N == 128, "rows 8 per warp, 8 x 16 columns per row");
@@ -471,7 +504,7 @@ static int launch(const StoreView& sv, int TT, const void* x, const void* B, con
                   const void* dt, float* y, cudaStream_t stream) {
   const bool wide = static_cast<long long>(sv.G) * sv.batch * 256 <= kPrepWideMaxThreads;
   auto prep = wide ? replay_verify_prep_kernel<P, N, T, 256> : replay_verify_prep_kernel<P, N, T, 128>;
-  const size_t psmem = static_cast<size_t>(sv.cap + kMaxDrafts) * N * sizeof(T);
+  const size_t psmem = static_cast<size_t>(sv.cap + 2 * TT) * N * sizeof(T);
   if (psmem > kSmemNoOptIn &&
       cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psmem)) !=
           cudaSuccess)
@@ -485,6 +518,9 @@ static int launch(const StoreView& sv, int TT, const void* x, const void* B, con
   if constexpr (RC == REPLAY_RC_NONE && N == 128) {
     kern = replay_verify_tc_kernel<P, N, T>;
     smem = tc_verify_smem<P, N, T>(TT, sv.cap);
+    // 4 CTAs per SM (up to 40 KB each at T = 8) need the largest shared-memory carveout
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+      return REPLAY_ECUDA;
   }
   if (smem > kSmemNoOptIn &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
