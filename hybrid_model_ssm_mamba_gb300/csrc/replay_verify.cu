@@ -28,6 +28,12 @@ namespace rssm {
 
 constexpr int kMaxDrafts = 8;
 constexpr int kVerifyBad = -1, kVerifyPlain = 0, kVerifyPrefold = 1;
+// FP32 checkpoint, dstate 128: the tensor-core kernel handles drafts in groups of 4 (its MMA
+// tiles have room for 4 drafts' C split in two), so it pays for whole groups; it takes the calls
+// whose draft count fills them (measured at batch 512, 8 heads: T = 4 60.8 vs 64.4 us, T = 8
+// 93.2 vs 95.1 us for the packed-FMA kernel), the packed-FMA kernel every other count (T = 1
+// 44.6 vs 51.8 us, T = 3 57.6 vs 58.3, T = 6 79.6 vs 83.8).
+inline bool verify_takes_tc(int TT) { return TT % 4 == 0; }
 
 // The prep's CTA size: 256 threads when the whole prep grid fits on the GPU at once with room
 // to spare (its serial per-head work then spreads over 8 warps), else 128 so that every prep
@@ -499,6 +505,198 @@ replay_verify_tc_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* 
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// FP32 checkpoint, dstate 128: every head's T outputs from one register tile, with few
+// instructions per value. Each warp takes 8 rows of the slab; lane (g, q) = (lane / 4, lane % 4)
+// holds row 8w + g, columns 16i + 4q .. 16i + 4q + 3 (i = 0..7), loaded with one 16-byte load
+// per i (each load of the warp reads 8 rows x 64 contiguous bytes). For draft j the lane forms
+// its part of h0 . C_j with packed FP32 FMAs (C_j in shared memory in FP32, the same 16 bytes
+// for the 8 lanes of a column quarter: one wavefront per load), scales it by Gamma_j, adds the
+// record terms c_j[s] x_s[row] of records s = q, q + 4, ... (x staged in shared memory with
+// rows padded to P + 8 values, so the 4 records a warp reads at once fall in distinct banks),
+// and two shuffles sum the row's four lanes. A warp-uniform loop over drafts; no warp-wide
+// reduction trees, no tensor-core operand splitting.
+template <int P, int N, class T>
+constexpr int kVerifyRecStride = P + 8;
+
+// Dynamic shared memory of the FP32-checkpoint verify kernel (bytes), in order: the fold
+// staging of a pre-fold; the drafts' C (input type); for bf16 inputs the same in FP32; the
+// drafts' x; the drafts' coefficients; this head's x ring by slot (padded rows).
+template <int P, int N, class T>
+constexpr size_t ffma_verify_smem(int TT, int cap) {
+  return fold_staging_bytes<P, N>(cap) + static_cast<size_t>(TT) * N * sizeof(T) +
+         (sizeof(T) == 4 ? 0 : static_cast<size_t>(TT) * N * sizeof(float)) +
+         static_cast<size_t>(TT) * kVerifyRecStride<P, N, T> * sizeof(T) +
+         align128(static_cast<size_t>(TT) * (cap + 1) * sizeof(float)) +
+         static_cast<size_t>(cap) * kVerifyRecStride<P, N, T> * sizeof(T);
+}
+
+template <int P, int N, class T>
+__global__ void __launch_bounds__(kThreads, 4)
+replay_verify_ffma_kernel(StoreView sv, int TT, const T* __restrict__ x, const T* __restrict__ B,
+                          const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
+  static_assert(P == 64 && N == 128, "rows 8 per warp, 8 x 16 columns per row");
+  constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC, XS = kVerifyRecStride<P, N, T>;
+  extern __shared__ float4 smem4[];
+  __shared__ float s_red[kWarps];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = lane & 3;
+  const int H = sv.H, G = sv.G, cap = sv.cap;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int h = g * sv.hpg + blockIdx.x;
+  const int slab = b * H + h;
+  const int row = warp * 8 + (lane >> 2);
+  const T* xb = x + static_cast<size_t>(b) * TT * H * P + static_cast<size_t>(h) * P;  // draft j: + j H P
+  const T* cb = C + static_cast<size_t>(b) * TT * G * N + static_cast<size_t>(g) * N;  // draft j: + j G N
+  const T* bb = B + static_cast<size_t>(b) * TT * G * N + static_cast<size_t>(g) * N;
+  float* yb = y + static_cast<size_t>(b) * TT * H * P + static_cast<size_t>(h) * P;
+
+  // shared memory regions
+  char* p0 = reinterpret_cast<char*>(smem4) + fold_staging_bytes<P, N>(cap);
+  T* sq = reinterpret_cast<T*>(p0);  // [TT][N] drafts' C
+  p0 += static_cast<size_t>(TT) * N * sizeof(T);
+  float* sqf = reinterpret_cast<float*>(sq);  // [TT][N] drafts' C in FP32
+  if constexpr (sizeof(T) != 4) {
+    sqf = reinterpret_cast<float*>(p0);
+    p0 += static_cast<size_t>(TT) * N * sizeof(float);
+  }
+  T* sx = reinterpret_cast<T*>(p0);  // [TT][XS] drafts' x
+  p0 += static_cast<size_t>(TT) * XS * sizeof(T);
+  float* s_cf = reinterpret_cast<float*>(p0);  // [TT][cap + 1] drafts' coefficients
+  p0 += align128(static_cast<size_t>(TT) * (cap + 1) * sizeof(float));
+  T* s_rec = reinterpret_cast<T*>(p0);  // [cap][XS] this head's x ring, by slot
+
+  // Independent of the prep kernel: the lane's 32 checkpoint values, the drafts' C and x and
+  // the x ring in shared memory, and each thread's share of the drafts' records to append (x
+  // of this head, B of the group by the group's first head, dt) in registers.
+  float a[8][4];
+  {
+    const float* hr = sv.h0 + static_cast<size_t>(slab) * P * N + static_cast<size_t>(row) * N + 4 * q;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ldv_stream<4>(hr + 16 * i, a[i]);
+  }
+  for (int c = tid; c < TT * (BC + XC); c += kThreads) {
+    if (c < TT * BC) {
+      const int j = c / BC, off = (c - j * BC) * EPC;
+      cp_async16(sq + j * N + off, cb + static_cast<size_t>(j) * G * N + off);
+    } else {
+      const int c2 = c - TT * BC;
+      const int j = c2 / XC, off = (c2 - j * XC) * EPC;
+      cp_async16(sx + j * XS + off, xb + static_cast<size_t>(j) * H * P + off);
+    }
+  }
+  // This head's whole x ring, by slot: its committed records are among them whatever the
+  // ring pointer turns out to be, and the prep does not write them, so the copy need not wait
+  // for the plan (the slots past the committed records are copied for nothing).
+  const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+  for (int c = tid; c < cap * XC; c += kThreads) {
+    const int slot = c / XC, off = (c - slot * XC) * EPC;
+    cp_async16(s_rec + slot * XS + off, ring.x + c * EPC);
+  }
+  cp_async_commit();
+  const int nxc = TT * XC, nbc = blockIdx.x == 0 ? TT * BC : 0, napp = nxc + nbc + TT;
+  uint4 app[2];
+  T appdt[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int c = tid + r * kThreads;
+    if (c < nxc) {
+      const int j = c / XC, off = (c - j * XC) * EPC;
+      app[r] = *reinterpret_cast<const uint4*>(xb + static_cast<size_t>(j) * H * P + off);
+    } else if (c < nxc + nbc) {
+      const int c2 = c - nxc, j = c2 / BC, off = (c2 - j * BC) * EPC;
+      app[r] = *reinterpret_cast<const uint4*>(bb + static_cast<size_t>(j) * G * N + off);
+    } else if (c < napp) {
+      appdt[r] = dt[(static_cast<size_t>(b) * TT + (c - nxc - nbc)) * H + h];
+    }
+  }
+  const float Dh = sv.D[h];
+
+  griddep_wait();  // plan and coefficients of this call are written
+  // the plan and this thread's share of the drafts' coefficients in one round trip
+  const int cs = cap + 1;
+  const float* cf = sv.coef + static_cast<size_t>(slab) * (sv.tmax + 1) * cs;
+  const float cfv = tid < TT * cs ? cf[cs + tid] : 0.f;
+  const int4 pl = sv.plan[b];
+  if (pl.z == kVerifyBad) {
+    cp_async_wait_all();
+    for (int j = 0; j < TT; ++j)
+      if (tid < P) yb[static_cast<size_t>(j) * H * P + tid] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const int start = pl.x, n = pl.y;
+  const bool prefold = pl.z == kVerifyPrefold;
+  const int start2 = prefold ? ring_slot(start, n, cap) : start;
+  const int n2 = prefold ? 0 : n;
+  // the drafts' records go to the ring beyond the committed ones; the pointer stays
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int c = tid + r * kThreads;
+    if (c < nxc) {
+      const int j = c / XC, off = (c - j * XC) * EPC;
+      *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(ring_slot(start2, n2 + j, cap)) * P + off) = app[r];
+    } else if (c < nxc + nbc) {
+      const int c2 = c - nxc, j = c2 / BC, off = (c2 - j * BC) * EPC;
+      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(ring_slot(start2, n2 + j, cap)) * N + off) = app[r];
+    } else if (c < napp) {
+      const int j = c - nxc - nbc;
+      ring.dt[ring_slot(start2, n2 + j, cap)] = appdt[r];
+    }
+  }
+
+  if (prefold) {  // a flush of the committed records, in the one-tile layout, then reload
+    using TL = Tile<P, N>;
+    float hv[TL::RPW][TL::E];
+    load_tile_f32<P, N>(sv.h0 + static_cast<size_t>(slab) * P * N, warp, lane, hv);
+    float* sm_u = reinterpret_cast<float*>(smem4);
+    float* sm_b = sm_u + cap * P;
+    auto xf = [&](int s) { return ring.x + static_cast<size_t>(ring_slot(start, s, cap)) * P; };
+    auto bfn = [&](int s) { return ring.b + static_cast<size_t>(ring_slot(start, s, cap)) * N; };
+    stage_weighted<P, N, T>(xf, bfn, cf, n, sm_u, sm_b);
+    __syncthreads();
+    fold_staged<P, N>(sm_u, sm_b, n, cf[cap], hv);
+    write_checkpoint<P, N, REPLAY_RC_NONE>(sv, slab, s_red, hv, pl.w);
+    __syncthreads();  // the new checkpoint is written (and visible to the block)
+    const float* hr = sv.h0 + static_cast<size_t>(slab) * P * N + static_cast<size_t>(row) * N + 4 * q;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // L2 reads: the block's own writes of the new checkpoint
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(hr + 16 * i));
+      a[i][0] = v.x; a[i][1] = v.y; a[i][2] = v.z; a[i][3] = v.w;
+    }
+  }
+
+  if (tid < TT * cs) s_cf[tid] = cfv;
+  for (int i = tid + kThreads; i < TT * cs; i += kThreads) s_cf[i] = cf[cs + i];
+  cp_async_wait_all();
+  __syncthreads();
+  if constexpr (sizeof(T) != 4) {
+    for (int e = tid; e < TT * N; e += kThreads) sqf[e] = to_f(sq[e]);
+    __syncthreads();
+  }
+
+  for (int j = 0; j < TT; ++j) {
+    const float* cj = s_cf + j * cs;
+    const float4* c4 = reinterpret_cast<const float4*>(sqf + j * N + 4 * q);
+    float2 ha = make_float2(0.f, 0.f), hb = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 c = c4[4 * i];  // columns 16i + 4q .. 16i + 4q + 3 of C_j
+      ha = __ffma2_rn(make_float2(a[i][0], a[i][1]), make_float2(c.x, c.y), ha);
+      hb = __ffma2_rn(make_float2(a[i][2], a[i][3]), make_float2(c.z, c.w), hb);
+    }
+    float v = cj[cap] * ((ha.x + ha.y) + (hb.x + hb.y));
+    const int k = n2 + j + 1;  // records draft j sees: the n2 committed ones, then drafts 0..j
+    for (int s = q; s < k; s += 4) {
+      const T xs = s < n2 ? s_rec[ring_slot(start2, s, cap) * XS + row] : sx[(s - n2) * XS + row];
+      v = fmaf(cj[s], to_f(xs), v);
+    }
+    v += __shfl_xor_sync(kFull, v, 1);
+    v += __shfl_xor_sync(kFull, v, 2);
+    if (q == 0) yb[static_cast<size_t>(j) * H * P + row] = fmaf(Dh, to_f(sx[j * XS + row]), v);
+  }
+}
+
 template <int P, int N, class T, int RC>
 static int launch(const StoreView& sv, int TT, const void* x, const void* B, const void* C,
                   const void* dt, float* y, cudaStream_t stream) {
@@ -516,8 +714,13 @@ static int launch(const StoreView& sv, int TT, const void* x, const void* B, con
   size_t smem = fold_staging_bytes<P, N>(sv.cap) + static_cast<size_t>(TT) * (P + N) * sizeof(T) +
                 static_cast<size_t>(TT) * (sv.cap + 1) * sizeof(float);
   if constexpr (RC == REPLAY_RC_NONE && N == 128) {
-    kern = replay_verify_tc_kernel<P, N, T>;
-    smem = tc_verify_smem<P, N, T>(TT, sv.cap);
+    if (!verify_takes_tc(TT)) {
+      kern = replay_verify_ffma_kernel<P, N, T>;
+      smem = ffma_verify_smem<P, N, T>(TT, sv.cap);
+    } else {
+      kern = replay_verify_tc_kernel<P, N, T>;
+      smem = tc_verify_smem<P, N, T>(TT, sv.cap);
+    }
     // 4 CTAs per SM (up to 40 KB each at T = 8) need the largest shared-memory carveout
     if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return REPLAY_ECUDA;
