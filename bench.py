@@ -363,6 +363,11 @@ def run_replay(args, rank, world, local_rank):
             v["nonflush_speedup_vs_fp32"] = fp32_nf_us / v["nonflush_launch_us"]
             v["window_speedup_vs_fp32"] = fp32_window_us / v["window_us"]
         extra["speculative"] = run_speculative(torch, R)
+        keep = ("replay_verify_commit_us", "snapshot_verify_commit_us", "conventional_step_us",
+                "replay_speedup_vs_snapshot", "replay_vs_standard_step")
+        extra["speculative"]["by_drafts"] = {
+            f"T{T}": {k: round(v, 3) for k, v in run_speculative(torch, R, T=T).items() if k in keep}
+            for T in (1, 8)}
         # the batch x window sweep of the small layer (fewer tokens than --sweep) and the
         # 40-layer stack, compact: speed-up of replay over the conventional step per config
         sw = run_sweep(torch, R, tokens=128)
