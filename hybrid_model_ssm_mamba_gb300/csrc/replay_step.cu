@@ -477,6 +477,202 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
 }
 
 // ---------------------------------------------------------------------------------------
+// replay_step_e4m3_mma_kernel: the non-flush step of an E4M3 read copy at dstate 128 with the
+// codes fed to the tensor cores as they are stored (`mma.sync` m16n8k32, E4M3 x E4M3 -> FP32):
+// no code is decoded by an instruction. C must enter as E4M3 too, so it is split into 8 terms,
+// one per MMA column: with s0 the power of two that brings max |C| below 256, r_0 = s0 C,
+// t_j = e4m3(r_j) (round to nearest even) and r_{j+1} = 16 (r_j - t_j), every step exact in
+// FP32, so s0 C = sum_j t_j 16^-j up to 2^-33 of its largest value. Column j of the MMA result
+// is then codes . t_j, products exact, and the row's h0 . C is scale / s0 * sum_j D[.][j] 16^-j.
+// The CTA takes HR heads of a group (one bulk copy of their codes), two warps per head, 32
+// rows each as two 16-row tiles. The MMA's k order is permuted so that lane (g, q) = (lane / 4,
+// lane % 4) reads one contiguous 32-byte piece of each row it needs (two 16-byte loads): in
+// k-tile kt, MMA k index 4q + i is column 32q + 8kt + i and 16 + 4q + i is column
+// 32q + 8kt + 4 + i, for A (the codes) and B (the C terms) alike. The k-tiles' partial sums
+// leave the accumulators after every MMA and add up in FP32. Lane (g, q) holds terms 2q and
+// 2q + 1 of rows g and g + 8: it weights them, adds its share of the record terms (records q,
+// q + 4, ... from x staged in shared memory by cp.async beside the copy) and two shuffles sum
+// the row's four lanes.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const unsigned (&a)[4], unsigned b0, unsigned b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Dynamic shared memory of the E4M3 tensor-core read kernel: the HR copy slabs, the records' x
+// of the HR heads ([HR][cap][P + 8], padded rows), their coefficients ([HR][cap + 1]).
+template <int P, int N, class T, int HR>
+constexpr size_t e4m3_mma_smem(int cap) {
+  return static_cast<size_t>(HR) * P * N + static_cast<size_t>(HR) * cap * (P + 8) * sizeof(T) +
+         static_cast<size_t>(HR) * (cap + 1) * sizeof(float);
+}
+
+template <int P, int N, class T, int HR>
+__global__ void __launch_bounds__(kThreads, 4)
+replay_step_e4m3_mma_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
+                            const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
+  static_assert(P == 64 && N == 128 && HR * 2 == kWarps, "two warps per head, 64 x 128 slabs");
+  constexpr int RC = REPLAY_RC_FP8E4M3;
+  constexpr int EPC = 16 / sizeof(T), XC = P / EPC, BC = N / EPC, XS = P + 8;
+  constexpr unsigned SLAB_BYTES = P * N;
+  extern __shared__ float4 smem4[];
+  __shared__ float s_red[kWarps];
+  __shared__ __align__(16) uint8_t s_terms[8][N];
+  __shared__ float s_inv;
+  __shared__ __align__(8) unsigned long long s_bar;
+  __shared__ int s_landed;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, q = lane & 3;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int hfirst = g * sv.hpg + blockIdx.x * HR;
+  const int slab0 = b * sv.H + hfirst;
+  const int cap = sv.cap;
+  const size_t bo = (static_cast<size_t>(b) * sv.G + g) * N;
+  const uint8_t* s_rc = reinterpret_cast<const uint8_t*>(smem4);
+  if (tid == 0) {
+    mbar_init(&s_bar);
+    bulk_load(smem4, static_cast<const uint8_t*>(sv.rc) + static_cast<size_t>(slab0) * SLAB_BYTES,
+              HR * SLAB_BYTES, &s_bar);
+  }
+  // C's 8 E4M3 terms (two threads per column compute the CTA-wide max |C|; one builds the terms)
+  {
+    const float c = to_f(C[bo + (tid & (N - 1))]);
+    const float m = warp_max(fabsf(c));
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    float cmax = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) cmax = fmaxf(cmax, s_red[w]);
+    if (tid < N) {
+      const int ce = cmax > 0.f ? max(((__float_as_int(cmax) >> 23) & 0xff) - 127, -110) : 0;
+      float r = c * __int_as_float((127 + 7 - ce) << 23);  // |r| < 256
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const unsigned short t2 = static_cast<unsigned short>(
+            __nv_cvt_float2_to_fp8x2(make_float2(r, 0.f), __NV_SATFINITE, __NV_E4M3));
+        s_terms[j][tid] = static_cast<uint8_t>(t2 & 0xffu);
+        r = (r - e4m3x2_to_float2(t2).x) * 16.f;
+      }
+      if (tid == 0) s_inv = __int_as_float((127 - 7 + ce) << 23);  // 1 / s0
+    }
+  }
+  __syncthreads();
+  const float inv_s0 = s_inv;
+  unsigned bt[4][2];  // B fragments: term gq at the lane's columns, per k-tile
+#pragma unroll
+  for (int kt = 0; kt < 4; ++kt) {
+    const uint2 w = *reinterpret_cast<const uint2*>(&s_terms[gq][32 * q + 8 * kt]);
+    bt[kt][0] = w.x;
+    bt[kt][1] = w.y;
+  }
+  // the weights of the lane's two terms, 16^-2q and 16^-(2q+1)
+  const float w0 = __int_as_float((127 - 8 * q) << 23), w1 = __int_as_float((127 - 8 * q - 4) << 23);
+
+  griddep_wait();  // plan and coefficients of this step are written
+  griddep_launch_dependents();  // after the wait: the next step's prep may start
+  const int4 pl = sv.plan[b];
+  const int start = pl.x, n = pl.y, k = n + 1;
+  T* s_x = reinterpret_cast<T*>(smem4 + HR * SLAB_BYTES / 16);  // [HR][cap][XS]
+  float* s_cf = reinterpret_cast<float*>(s_x + static_cast<size_t>(HR) * cap * XS);  // [HR][cap + 1]
+  const bool nonflush = pl.z == kPlanNonFlush;
+  if (nonflush) {  // the k records' x and the coefficients, beside the copy: one round trip
+    for (int c = tid; c < HR * k * XC; c += kThreads) {
+      const int hh = c / (k * XC), r = c - hh * k * XC, s = r / XC, off = (r - s * XC) * EPC;
+      const T* src = s < n ? slab_ring<P, N, T>(sv, b, hfirst + hh, g).x + static_cast<size_t>(ring_slot(start, s, cap)) * P
+                           : x + static_cast<size_t>(slab0 + hh) * P;
+      cp_async16(s_x + (static_cast<size_t>(hh) * cap + s) * XS + off, src + off);
+    }
+    for (int c = tid; c < HR * (cap + 1); c += kThreads)
+      s_cf[c] = sv.coef[static_cast<size_t>(slab0) * (cap + 1) + c];  // the HR slabs' rows are consecutive
+    cp_async_commit();
+  }
+  // The copy must have landed before it is read or the CTA exits (bounded wait, see the FP32
+  // read kernel).
+  if (tid == 0) {
+    const bool ok = mbar_wait(&s_bar, 0, kCopyWaitNs);
+    if (!ok) {
+      set_status(sv.status, REPLAY_DEV_COPY_TIMEOUT);
+      mbar_wait(&s_bar, 0, kCopyWaitNs);
+    }
+    s_landed = ok;
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  if (!s_landed || pl.z == kPlanBad) {
+    for (int hh = 0; hh < HR; ++hh)
+      if (tid < P) y[static_cast<size_t>(slab0 + hh) * P + tid] = __int_as_float(0x7fc00000);
+    return;
+  }
+
+  if (nonflush) {
+    const int hh = warp >> 1, half = warp & 1;
+    const int h = hfirst + hh, slab = slab0 + hh;
+    const size_t xo = static_cast<size_t>(slab) * P;
+    const float* cf = s_cf + hh * (cap + 1);
+    const T* sxh = s_x + static_cast<size_t>(hh) * cap * XS;
+    float part[4];  // rows 32 half + 16 t + 8 u + gq, index 2t + u
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int r0 = 32 * half + 16 * t + gq;
+      const uint8_t* row0 = s_rc + hh * SLAB_BYTES + r0 * N + 32 * q;
+      const uint4 lo0 = *reinterpret_cast<const uint4*>(row0), hi0 = *reinterpret_cast<const uint4*>(row0 + 16);
+      const uint4 lo1 = *reinterpret_cast<const uint4*>(row0 + 8 * N), hi1 = *reinterpret_cast<const uint4*>(row0 + 8 * N + 16);
+      const unsigned ra[8] = {lo0.x, lo0.y, lo0.z, lo0.w, hi0.x, hi0.y, hi0.z, hi0.w};
+      const unsigned rb[8] = {lo1.x, lo1.y, lo1.z, lo1.w, hi1.x, hi1.y, hi1.z, hi1.w};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        const unsigned a[4] = {ra[2 * kt], rb[2 * kt], ra[2 * kt + 1], rb[2 * kt + 1]};
+        mma_e4m3_16832(d, a, bt[kt][0], bt[kt][1]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += d[e];
+      }
+      part[2 * t] = fmaf(acc[1], w1, acc[0] * w0);      // row r0: terms 2q, 2q + 1
+      part[2 * t + 1] = fmaf(acc[3], w1, acc[2] * w0);  // row r0 + 8
+    }
+    const float gs = cf[cap] * sv.scale[slab] * inv_s0;  // Gamma_k, the slab scale, 1 / s0
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = 32 * half + 16 * (i >> 1) + 8 * (i & 1) + gq;
+      float e = 0.f;  // the record terms of this lane's records q, q + 4, ...
+      for (int s = q; s < k; s += 4) e = fmaf(cf[s], to_f(sxh[s * XS + row]), e);
+      part[i] = fmaf(gs, part[i], e);
+      part[i] += __shfl_xor_sync(kFull, part[i], 1);
+      part[i] += __shfl_xor_sync(kFull, part[i], 2);
+    }
+    // lane q writes its row q of the four: the warp's 32 rows in one 128-byte store
+    const int rq = 32 * half + 16 * (q >> 1) + 8 * (q & 1) + gq;
+    const float v = q == 0 ? part[0] : q == 1 ? part[1] : q == 2 ? part[2] : part[3];
+    y[xo + rq] = fmaf(sv.D[h], to_f(x[xo + rq]), v);
+    // this token's record: the warp pair's head
+    const int slot = ring_slot(start, n, cap);
+    const SlabRing<T> ring = slab_ring<P, N, T>(sv, b, h, g);
+    const int ht = tid & 63;  // thread of the head's warp pair
+    if (ht < XC) {
+      *reinterpret_cast<uint4*>(ring.x + static_cast<size_t>(slot) * P + ht * EPC) =
+          *reinterpret_cast<const uint4*>(x + xo + ht * EPC);
+    } else if (!sv.prep_appends && blockIdx.x == 0 && hh == 0 && ht < XC + BC) {
+      const int c = ht - XC;
+      *reinterpret_cast<uint4*>(ring.b + static_cast<size_t>(slot) * N + c * EPC) =
+          *reinterpret_cast<const uint4*>(B + bo + c * EPC);
+    } else if (!sv.prep_appends && ht == XC + BC) {
+      ring.dt[slot] = dt[slab];
+    }
+    return;
+  }
+
+  // flush (not expected): out of line, so that its registers do not weigh on the read path
+  float scl[HR];
+#pragma unroll
+  for (int hh = 0; hh < HR; ++hh) scl[hh] = sv.scale[slab0 + hh];
+  copy_read_flush<P, N, T, RC, HR>(sv, x, B, C, y, s_rc, scl, start, n, pl.w, s_red);
+}
+
+// ---------------------------------------------------------------------------------------
 // replay_step_read_kernel: the FP32-checkpoint step when the host knows that no sequence
 // flushes (the non-flush steps of a window). Such a step only reads, so its speed is the
 // bytes an SM keeps in flight. A register tile holds 32 KB per CTA and the register file
@@ -1319,6 +1515,16 @@ static int launch(const StoreView& base, int all_n, int parity, int overlap, con
     if (all_flush && !sv.shared && !sv.ckpt16)
       return pdl_launch(replay_step_read_kernel<P, N, T, true, RC>, dim3(sv.hpg, sv.G, sv.batch), flsmem,
                         stream, sv, tx, tB, tC, tdt, y);
+  }
+  if constexpr (RC == REPLAY_RC_FP8E4M3 && P == 64 && N == 128) {
+    constexpr int HR = 4;
+    if (all_n >= 0 && !all_flush && sv.hpg % HR == 0) {
+      if (cudaFuncSetAttribute(replay_step_e4m3_mma_kernel<P, N, T, HR>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+        return REPLAY_ECUDA;
+      return pdl_launch(replay_step_e4m3_mma_kernel<P, N, T, HR>, dim3(sv.hpg / HR, sv.G, sv.batch),
+                        e4m3_mma_smem<P, N, T, HR>(sv.cap), stream, sv, tx, tB, tC, tdt, y);
+    }
   }
   if constexpr (RC != REPLAY_RC_NONE && RC != REPLAY_RC_NVFP4) {
     constexpr int HPC = heads_per_cta<N, RC>();
