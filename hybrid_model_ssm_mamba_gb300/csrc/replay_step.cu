@@ -488,8 +488,8 @@ replay_step_copy_read_kernel(StoreView sv, const T* __restrict__ x, const T* __r
 // rows each as two 16-row tiles. The MMA's k order is permuted so that lane (g, q) = (lane / 4,
 // lane % 4) reads one contiguous 32-byte piece of each row it needs (two 16-byte loads): in
 // k-tile kt, MMA k index 4q + i is column 32q + 8kt + i and 16 + 4q + i is column
-// 32q + 8kt + 4 + i, for A (the codes) and B (the C terms) alike. The k-tiles' partial sums
-// leave the accumulators after every MMA and add up in FP32. Lane (g, q) holds terms 2q and
+// 32q + 8kt + 4 + i, for A (the codes) and B (the C terms) alike. A row's 128 products per
+// term accumulate over the 4 k-tiles in the MMA accumulators. Lane (g, q) holds terms 2q and
 // 2q + 1 of rows g and g + 8: it weights them, adds its share of the record terms (records q,
 // q + 4, ... from x staged in shared memory by cp.async beside the copy) and two shuffles sum
 // the row's four lanes.
@@ -510,7 +510,7 @@ constexpr size_t e4m3_mma_smem(int cap) {
 }
 
 template <int P, int N, class T, int HR>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 5)
 replay_step_e4m3_mma_kernel(StoreView sv, const T* __restrict__ x, const T* __restrict__ B,
                             const T* __restrict__ C, const T* __restrict__ dt, float* __restrict__ y) {
   static_assert(P == 64 && N == 128 && HR * 2 == kWarps, "two warps per head, 64 x 128 slabs");
@@ -546,15 +546,17 @@ replay_step_e4m3_mma_kernel(StoreView sv, const T* __restrict__ x, const T* __re
     float cmax = s_red[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) cmax = fmaxf(cmax, s_red[w]);
-    if (tid < N) {
+    if (tid < N / 2) {  // columns 2 tid, 2 tid + 1
       const int ce = cmax > 0.f ? max(((__float_as_int(cmax) >> 23) & 0xff) - 127, -110) : 0;
-      float r = c * __int_as_float((127 + 7 - ce) << 23);  // |r| < 256
+      const float s0 = __int_as_float((127 + 7 - ce) << 23);
+      float2 r = make_float2(to_f(C[bo + 2 * tid]) * s0, to_f(C[bo + 2 * tid + 1]) * s0);  // |r| < 256
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const unsigned short t2 = static_cast<unsigned short>(
-            __nv_cvt_float2_to_fp8x2(make_float2(r, 0.f), __NV_SATFINITE, __NV_E4M3));
-        s_terms[j][tid] = static_cast<uint8_t>(t2 & 0xffu);
-        r = (r - e4m3x2_to_float2(t2).x) * 16.f;
+        const unsigned short t2 =
+            static_cast<unsigned short>(__nv_cvt_float2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3));
+        *reinterpret_cast<unsigned short*>(&s_terms[j][2 * tid]) = t2;
+        const float2 tv = e4m3x2_to_float2(t2);
+        r = make_float2((r.x - tv.x) * 16.f, (r.y - tv.y) * 16.f);
       }
       if (tid == 0) s_inv = __int_as_float((127 - 7 + ce) << 23);  // 1 / s0
     }
@@ -579,8 +581,9 @@ replay_step_e4m3_mma_kernel(StoreView sv, const T* __restrict__ x, const T* __re
   float* s_cf = reinterpret_cast<float*>(s_x + static_cast<size_t>(HR) * cap * XS);  // [HR][cap + 1]
   const bool nonflush = pl.z == kPlanNonFlush;
   if (nonflush) {  // the k records' x and the coefficients, beside the copy: one round trip
-    for (int c = tid; c < HR * k * XC; c += kThreads) {
-      const int hh = c / (k * XC), r = c - hh * k * XC, s = r / XC, off = (r - s * XC) * EPC;
+    const int off = (tid % XC) * EPC;
+    for (int pr = tid / XC; pr < HR * k; pr += kThreads / XC) {  // (head, record) pairs
+      const int hh = pr / k, s = pr - hh * k;
       const T* src = s < n ? slab_ring<P, N, T>(sv, b, hfirst + hh, g).x + static_cast<size_t>(ring_slot(start, s, cap)) * P
                            : x + static_cast<size_t>(slab0 + hh) * P;
       cp_async16(s_x + (static_cast<size_t>(hh) * cap + s) * XS + off, src + off);
@@ -622,25 +625,26 @@ replay_step_e4m3_mma_kernel(StoreView sv, const T* __restrict__ x, const T* __re
       const uint4 lo1 = *reinterpret_cast<const uint4*>(row0 + 8 * N), hi1 = *reinterpret_cast<const uint4*>(row0 + 8 * N + 16);
       const unsigned ra[8] = {lo0.x, lo0.y, lo0.z, lo0.w, hi0.x, hi0.y, hi0.z, hi0.w};
       const unsigned rb[8] = {lo1.x, lo1.y, lo1.z, lo1.w, hi1.x, hi1.y, hi1.z, hi1.w};
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};  // 128 exact products per element, as 4 MMAs
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
         const unsigned a[4] = {ra[2 * kt], rb[2 * kt], ra[2 * kt + 1], rb[2 * kt + 1]};
-        mma_e4m3_16832(d, a, bt[kt][0], bt[kt][1]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += d[e];
+        mma_e4m3_16832(acc, a, bt[kt][0], bt[kt][1]);
       }
       part[2 * t] = fmaf(acc[1], w1, acc[0] * w0);      // row r0: terms 2q, 2q + 1
       part[2 * t + 1] = fmaf(acc[3], w1, acc[2] * w0);  // row r0 + 8
     }
     const float gs = cf[cap] * sv.scale[slab] * inv_s0;  // Gamma_k, the slab scale, 1 / s0
+    float e[4] = {0.f, 0.f, 0.f, 0.f};  // the record terms of this lane's records q, q + 4, ...
+    const T* xr = sxh + 32 * half + gq;
+    for (int s = q; s < k; s += 4) {
+      const float c = cf[s];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) e[i] = fmaf(c, to_f(xr[s * XS + 16 * (i >> 1) + 8 * (i & 1)]), e[i]);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int row = 32 * half + 16 * (i >> 1) + 8 * (i & 1) + gq;
-      float e = 0.f;  // the record terms of this lane's records q, q + 4, ...
-      for (int s = q; s < k; s += 4) e = fmaf(cf[s], to_f(sxh[s * XS + row]), e);
-      part[i] = fmaf(gs, part[i], e);
+      part[i] = fmaf(gs, part[i], e[i]);
       part[i] += __shfl_xor_sync(kFull, part[i], 1);
       part[i] += __shfl_xor_sync(kFull, part[i], 2);
     }
