@@ -561,6 +561,38 @@ def test_copy_reads_follow_the_decoded_copy(rc, batch, heads, groups, dtype, dst
     assert st.status() == 0
 
 
+def test_e4m3_reads_at_extreme_query_scales():
+    """The E4M3 copy read at dstate 128 splits each group's C into E4M3 terms under a power-of-two
+    scale taken from max |C|. Groups whose C is scaled by 1, 0, 1e-30, 1e30, 1e-20, 1e20, or has
+    one column 1e3 above the rest, still give the decoded copy's outputs within 1e-4 (FP32
+    inputs; 17 sequences x 64 heads, 8 groups: the large-call path)."""
+    shape = sg.LayerShape(17, 64, 64, 128, 8, "f32")
+    L, seed = 8, 33
+    st, A, D = make_store(shape, seed, L=L, read_copy=R.REPLAY_RC_FP8E4M3)
+    sel = np.array([0, 9, 16])
+    h0 = sg.initial_state(shape, seed)
+    st.load_state(torch.from_numpy(h0).cuda())
+    hread = _decoded_copy(st, R.REPLAY_RC_FP8E4M3, h0[sel])
+    scale = np.array([1.0, 0.0, 1e-30, 1e30, 1.0, 1e-20, 1e20, 1.0], dtype=np.float32)
+    y = torch.empty(17, 64, 64, device="cuda")
+    rec = {k: [] for k in ("x", "B", "dt")}
+    worst = 0.0
+    for t in range(L - 1):
+        d = sg.token_inputs(shape, seed, [t])
+        c32 = np.ascontiguousarray(d["C"].store[:, 0]).astype(np.float32) * scale[None, :, None]
+        c32[:, 4, 5] *= np.float32(1e3)  # group 4: one column far above the others
+        devs = [torch.from_numpy(np.ascontiguousarray(d[k].store[:, 0])).cuda() for k in ("x", "B")]
+        devs += [torch.from_numpy(c32).cuda(), torch.from_numpy(np.ascontiguousarray(d["dt"].store[:, 0])).cuda()]
+        st.step(*devs, y)
+        for k in ("x", "B", "dt"):
+            rec[k].append(d[k].f64[sel, 0])
+        ywin = window_output(hread, np.stack(rec["x"], 1), np.stack(rec["B"], 1), np.stack(rec["dt"], 1),
+                             c32[sel].astype(np.float64), A, D)
+        worst = max(worst, rel_vec_err(y[sel].cpu().numpy(), ywin, 2).max())
+    assert worst <= TOL, worst
+    assert st.status() == 0
+
+
 @pytest.mark.parametrize("rc,tol", [(R.REPLAY_RC_BF16, 5e-3), (R.REPLAY_RC_FP8E4M3, 5e-2),
                                     (R.REPLAY_RC_FP16, 1e-3), (R.REPLAY_RC_NVFP4, 5e-2)])
 @pytest.mark.parametrize("batch,heads,groups", [(4, 8, 2), (72, 128, 8)])
