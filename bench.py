@@ -359,8 +359,10 @@ def run_replay(args, rank, world, local_rank):
         extra["read_copy"] = run_read_copies(torch, R, dev)
         fp32_nf_us = float(launch_s[:, :-1].mean() * 1e6)
         fp32_window_us = elapsed / args.steps * 1e6
+        fp32_nf_window_us = (fp32_window_us - float(launch_s[:, -1].mean() * 1e6)) / (L - 1)
         for v in extra["read_copy"].values():   # the post's "non-flush kernel N x faster" figure
             v["nonflush_speedup_vs_fp32"] = fp32_nf_us / v["nonflush_launch_us"]
+            v["nonflush_speedup_vs_fp32_in_window"] = fp32_nf_window_us / v["nonflush_us_in_window"]
             v["window_speedup_vs_fp32"] = fp32_window_us / v["window_us"]
         extra["speculative"] = run_speculative(torch, R)
         keep = ("replay_verify_commit_us", "snapshot_verify_commit_us", "conventional_step_us",
@@ -531,11 +533,16 @@ def run_read_copies(torch, R, dev, steps=10):
         nf_bytes = sum(step_bytes(w, t, False, rc_bytes=rcb, slab_scale=slab_scale) for t in range(L - 1))
         fl_bytes = step_bytes(w, L - 1, True, rc_bytes=rcb, shared=bool(shared), slab_scale=slab_scale,
                               state_bytes=2 if ckpt else 4)
+        # back to back in a window the next call's prep overlaps this call's kernel, which an
+        # event pair around each call prevents: the window's non-flush calls on average
+        nf_window_us = (window_us - float(us[:, -1].mean())) / (L - 1)
         out[name] = {"tokens_per_s": w["batch"] * L / (window_us * 1e-6),
                      "window_us": window_us,
                      "nonflush_launch_us": float(us[:, :-1].mean()),
                      "flush_launch_us": float(us[:, -1].mean()),
+                     "nonflush_us_in_window": nf_window_us,
                      "nonflush_achieved_gbs": nf_bytes / (us[:, :-1].sum(axis=1).mean() * 1e-6) / 1e9,
+                     "nonflush_achieved_gbs_in_window": nf_bytes / ((L - 1) * nf_window_us * 1e-6) / 1e9,
                      "flush_achieved_gbs": fl_bytes / (us[:, -1].mean() * 1e-6) / 1e9}
         assert st.status() == 0
         st.close()
