@@ -537,7 +537,8 @@ replay_step_e4m3_mma_kernel(StoreView sv, const T* __restrict__ x, const T* __re
     bulk_load(smem4, static_cast<const uint8_t*>(sv.rc) + static_cast<size_t>(slab0) * SLAB_BYTES,
               HR * SLAB_BYTES, &s_bar);
   }
-X
+  // C's 8 E4M3 terms (two threads per column find the CTA-wide max |C|; one thread per two
+  // columns builds their terms)
   {
     const float c = to_f(C[bo + (tid & (N - 1))]);
     const float m = warp_max(fabsf(c));
