@@ -397,11 +397,11 @@ def test_verify_workload_shape(rc):
     assert st.status() == 0
 
 
-@pytest.mark.parametrize("T", [1, 5, 8])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_verify_draft_counts_bf16(T):
-    """Draft counts below, across and at the top of the tensor-core kernel's groups of four
-    drafts, bf16 inputs, 4 groups; commits leave up to L - 1 + T records so that verifies
-    also pre-fold. Every output and the final state against the oracle."""
+    """Every draft count: the packed-FMA kernel (T not a multiple of 4) and the tensor-core
+    kernel (T = 4, 8), bf16 inputs, 4 groups; commits leave up to L - 1 + T records so that
+    verifies also pre-fold. Every output and the final state against the oracle."""
     shape = sg.LayerShape(6, 16, 64, 128, 4, "bf16")
     L = 8
     st, A, D = make_store(shape, 13, L=L, T=T)
