@@ -691,20 +691,43 @@ def _decoded_nvfp4(st, seqs):
     return out
 
 
-@pytest.mark.parametrize("batch,heads,groups,dtype", [(4, 8, 2, "f32"), (72, 128, 8, "bf16")])
-def test_fp16_sr_checkpoint_with_nvfp4_reads(batch, heads, groups, dtype):
-    """The recurrence checkpoint in FP16 with stochastic rounding, and a separate NVFP4 read
-    copy cast from the same FP32 fold (post, "Benefit 3": NVFP4 reads with an FP16 recurrence).
-    Checked: flush outputs and the FP16 checkpoints follow the oracle that rounds its state
-    stochastically after every window, with the same draws (up to rare flips between FP32 and
-    FP64 states); non-flush outputs equal the window evaluated in FP64 from the device's
-    decoded NVFP4 copy, within 1e-4; the copy is the NVFP4 encoding of the flush's unrounded
-    state (up to the same rare flips), not of the FP16 checkpoint."""
+def _device_copy(st, rc, seqs):
+    """The values non-flush steps read from the store's read copy, decoded from the device's
+    own bytes (and scales) by the oracle's decoders."""
+    if rc == R.REPLAY_RC_NVFP4:
+        return _decoded_nvfp4(st, seqs)
+    if rc == R.REPLAY_RC_BF16:
+        return st.region("rc")[seqs].float().cpu().numpy().astype(np.float64)
+    codes = st.region("rc").cpu().numpy()[seqs]
+    sc = st.region("scale").cpu().numpy()[seqs].astype(np.float32)
+    return (F.e4m3_decode(codes).astype(np.float32) * sc[:, :, None, None]).astype(np.float64)
+
+
+def _round_copy(rc, h32):
+    """The read copy the format gives the FP32 states h32 [b, H, P, N], read back."""
+    if rc == R.REPLAY_RC_NVFP4:
+        return F.nvfp4_round_state(h32)
+    if rc == R.REPLAY_RC_BF16:
+        return F.bf16_round_state(h32)
+    return F.e4m3_round_state(h32)
+
+
+@pytest.mark.parametrize("batch,heads,groups,dtype,rc", [
+    (4, 8, 2, "f32", R.REPLAY_RC_NVFP4), (72, 128, 8, "bf16", R.REPLAY_RC_NVFP4),
+    (72, 128, 8, "bf16", R.REPLAY_RC_BF16), (72, 128, 8, "f32", R.REPLAY_RC_FP8E4M3),
+    (4, 8, 2, "bf16", R.REPLAY_RC_FP8E4M3)])
+def test_fp16_sr_checkpoint_with_nvfp4_reads(batch, heads, groups, dtype, rc):
+    """The recurrence checkpoint in FP16 with stochastic rounding, and a separate read copy
+    (NVFP4, bf16 or E4M3) cast from the same FP32 fold (post, "Benefit 3": NVFP4 reads with an
+    FP16 recurrence). Checked: flush outputs and the FP16 checkpoints follow the oracle that
+    rounds its state stochastically after every window, with the same draws (up to rare flips
+    between FP32 and FP64 states); non-flush outputs equal the window evaluated in FP64 from the
+    device's decoded copy, within 1e-4; the copy is the encoding of the flush's unrounded state
+    (up to the same rare flips), not of the FP16 checkpoint."""
     shape = sg.LayerShape(batch, heads, 64, 128, groups, dtype)
     L, steps, seed = 8, 24, 27
     A, D = sg.head_params(heads, seed)
-    cfg = R.ReplayConfig(batch, heads, 64, 128, groups, L, 0, DTYPE[dtype], R.REPLAY_RC_NVFP4, 0,
-                         R.REPLAY_CKPT_F16_SR)
+    cfg = R.ReplayConfig(batch, heads, 64, 128, groups, L, 0, DTYPE[dtype], rc, 0, R.REPLAY_CKPT_F16_SR)
     st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
     sel = np.array([0, batch - 1])
     A64, D64 = A.astype(float), D.astype(float)
@@ -732,11 +755,11 @@ def test_fp16_sr_checkpoint_with_nvfp4_reads(batch, heads, groups, dtype):
         h16 = st.region("h0").float().cpu().numpy()[sel]
         d = np.abs(h16 - rounded.h) / np.abs(rounded.h).max(axis=(2, 3), keepdims=True)
         assert d.max() <= 2 * 2.0 ** -10 and (d > 1e-5).mean() <= 1e-3, (t, d.max(), (d > 1e-5).mean())
-        hread = _decoded_nvfp4(st, sel)
-        want = np.stack([F.nvfp4_round_state(pre.h[i:i + 1])[0] for i in range(2)])
+        hread = _device_copy(st, rc, sel)
+        want = np.stack([_round_copy(rc, pre.h[i:i + 1])[0] for i in range(2)])
         flips = np.abs(hread - want) > 1e-6 * np.abs(want).max()
         assert flips.mean() <= 1e-3, (t, flips.mean())
-        from_ckpt = F.nvfp4_round_state(h16)
+        from_ckpt = _round_copy(rc, h16)
         assert np.abs(hread - from_ckpt).max() > 0                 # cast from FP32, not from FP16
         pre = Mamba2Decoder(A64, D64, groups, rounded.h.copy())   # the next window starts from it
         rec = {k: [] for k in ("x", "B", "dt")}
