@@ -426,6 +426,33 @@ def test_verify_draft_counts_bf16(T):
     assert st.status() == 0
 
 
+@pytest.mark.parametrize("rc", [R.REPLAY_RC_BF16, R.REPLAY_RC_FP16, R.REPLAY_RC_FP8E4M3, R.REPLAY_RC_NVFP4])
+def test_verify_reads_the_decoded_copy(rc):
+    """Verify with a read copy evaluates every draft from the copy: six verify + commit calls
+    (no pre-fold: L 32, T 4) against the oracle started from the copy's decoded values of the
+    loaded state, within 1e-4 (40 sequences x 32 heads, 4 groups, bf16 inputs)."""
+    shape = sg.LayerShape(40, 32, 64, 128, 4, "bf16")
+    T, L, seed = 4, 32, 19
+    st, A, D = make_store(shape, seed, L=L, T=T, read_copy=rc)
+    sel = np.array([0, 21, 39])
+    h0 = sg.initial_state(shape, seed)
+    st.load_state(torch.from_numpy(h0).cuda())
+    hdec = F.nvfp4_round_state(h0[sel]) if rc == R.REPLAY_RC_NVFP4 else _decoded_copy(st, rc, h0[sel])
+    orc = Mamba2Decoder(A, D, 4, hdec)
+    y = torch.empty(40, T, 32, 64, device="cuda")
+    worst = 0.0
+    for call in range(6):
+        devs, f64 = draft_device(shape, seed, call, T)
+        st.verify(T, *devs, y)
+        f64s = [a[sel] for a in f64]
+        worst = max(worst, rel_vec_err(y[sel].cpu().numpy(), orc.verify(*f64s), 3).max())
+        acc = sg.accept_lengths(40, T, seed, call)
+        st.commit(torch.from_numpy(acc).cuda())
+        orc.commit(acc[sel], f64s[0], f64s[1], f64s[3])
+    assert worst <= TOL, worst
+    assert st.status() == 0
+
+
 def test_bad_accept_sets_status_and_commits_nothing():
     shape = sg.LayerShape(2, 2, 64, 128, 1, "f32")
     st, _, _ = make_store(shape, 13, L=4, T=2)
