@@ -426,14 +426,19 @@ def test_verify_draft_counts_bf16(T):
     assert st.status() == 0
 
 
-@pytest.mark.parametrize("rc", [R.REPLAY_RC_BF16, R.REPLAY_RC_FP16, R.REPLAY_RC_FP8E4M3, R.REPLAY_RC_NVFP4])
-def test_verify_reads_the_decoded_copy(rc):
-    """Verify with a read copy evaluates every draft from the copy: six verify + commit calls
-    (no pre-fold: L 32, T 4) against the oracle started from the copy's decoded values of the
-    loaded state, within 1e-4 (40 sequences x 32 heads, 4 groups, bf16 inputs)."""
+@pytest.mark.parametrize("rc,shared", [(R.REPLAY_RC_BF16, 0), (R.REPLAY_RC_FP16, 0), (R.REPLAY_RC_FP8E4M3, 0),
+                                       (R.REPLAY_RC_NVFP4, 0), (R.REPLAY_RC_BF16, 1), (R.REPLAY_RC_FP8E4M3, 1)])
+def test_verify_reads_the_decoded_copy(rc, shared):
+    """Verify with a read copy (or a shared low-precision checkpoint) evaluates every draft
+    from the copy: six verify + commit calls (no pre-fold: L 32, T 4) against the oracle
+    started from the copy's decoded values of the loaded state, within 1e-4 (40 sequences x
+    32 heads, 4 groups, bf16 inputs)."""
     shape = sg.LayerShape(40, 32, 64, 128, 4, "bf16")
     T, L, seed = 4, 32, 19
-    st, A, D = make_store(shape, seed, L=L, T=T, read_copy=rc)
+    A, D = sg.head_params(32, seed)
+    cfg = R.ReplayConfig(40, 32, 64, 128, 4, L, T, DTYPE["bf16"], rc, shared)
+    st = R.ReplayStore(cfg, torch.from_numpy(A), torch.from_numpy(D))
+    A, D = A.astype(np.float64), D.astype(np.float64)
     sel = np.array([0, 21, 39])
     h0 = sg.initial_state(shape, seed)
     st.load_state(torch.from_numpy(h0).cuda())
